@@ -1,0 +1,421 @@
+"""Benchmark of the paged-decode hot path on GB300.
+
+One step = pa_kv_cache_write of the batch's new tokens + pa_decode (split
+partitions + log-sum-exp combine) over the LLaMA-13B-shaped batch: 38
+sequences, 40 heads, head_dim 128, block_size 16, context lengths uniform in
+[128, 2048], fp16 N(0,1) synthetic data.  The metric is algorithmic HBM
+GB/s (K+V rows attended + q + out + table/length reads + the cache write's
+read and write), plus attended tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU (torchrun): every rank runs its own independent batch (decode
+sequences are independent; no collective on the data path); value = bytes
+of all ranks / max-over-ranks time, scaling "weak".
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged-decode KV HBM GB/s (% of ~8 TB/s) and attended tokens/s, 1×GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+# dram__bytes_read.sum + dram__bytes_write.sum per pa_decode call (partition +
+# combine kernels) from one ncu capture of the 38-sequence batch, keyed by the
+# hash of the decode source it was taken on; null once the source changes.
+DECODE_TRAFFIC = {}
+
+
+def src_hash(name):
+    p = os.path.join(ROOT, "paged_kv_cache_172_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload and byte accounting
+# ---------------------------------------------------------------------------
+def decode_bytes(ctx, B, H, D, bs):
+    ctx = np.asarray(ctx, dtype=np.int64)
+    kv = int(ctx.sum()) * H * D * 2 * 2
+    qo = 2 * B * H * D * 2
+    tables = int(sum(-(-int(c) // bs) for c in ctx)) * 4 + B * 4
+    return kv + qo + tables
+
+
+def write_bytes(T, H, D):
+    return 2 * (2 * T * H * D * 2) + T * 8
+
+
+def make_workload(device, seed=1):
+    from paged_kv_cache_172_gb300 import workloads
+    return workloads.llama13b_decode(seed=seed, device=device)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, rank, world, local_rank):
+    import paged_kv_cache_172_gb300 as pk
+    from paged_kv_cache_172_gb300 import build_lib
+    from paged_kv_cache_172_gb300.session import DecodeSession
+
+    build_lib.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    batch = make_workload(dev, seed=1 + rank)
+    B, H, D, bs = batch.B, batch.H, batch.D, batch.block_size
+    ctx = batch.context_lens.cpu().numpy()
+    max_ctx = 2048
+    pt = args.partition_tokens or pk.pa_decode_partition_tokens(B, H, bs, max_ctx)
+    ws_bytes = pk.pa_decode_workspace_size(B, H, D, bs, max_ctx, pt)
+    ws = torch.empty(max(ws_bytes // 4, 1) + 4, dtype=torch.float32, device=dev)
+    out = torch.empty_like(batch.q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        pk.pa_kv_cache_write(batch.k_new, batch.v_new, batch.slot_mapping, batch.k_cache,
+                             batch.v_cache, status=status, stream=stream)
+        pk.pa_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                     batch.context_lens, batch.scale, max_ctx, out=out, partition_tokens=pt,
+                     workspace=ws, status=status, stream=stream)
+
+    n_parts = -(-max_ctx // pt)
+    launches_per_step = 1 + 1 + (1 if n_parts > 1 else 0)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(float(i))  # evict the previous step from L2 (untimed)
+                e0, e1, e2 = ev[i]
+                e0.record(stream)
+                pk.pa_kv_cache_write(batch.k_new, batch.v_new, batch.slot_mapping,
+                                     batch.k_cache, batch.v_cache, status=status, stream=stream)
+                e1.record(stream)
+                pk.pa_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                             batch.context_lens, batch.scale, max_ctx, out=out,
+                             partition_tokens=pt, workspace=ws, status=status, stream=stream)
+                e2.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    wr_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the timed region")
+    total_ms = sum(step_ms)
+
+    # -- end to end: host buffers, copies inside the timed region ---------------
+    sess = DecodeSession(batch.k_cache, batch.v_cache, B, batch.block_tables.shape[1], max_ctx,
+                         batch.scale, partition_tokens=pt)
+    host = sess.host_buffers()
+    host["q"].copy_(batch.q)
+    host["k_new"].copy_(batch.k_new)
+    host["v_new"].copy_(batch.v_new)
+    host["slots"].copy_(batch.slot_mapping)
+    host["context_lens"].copy_(batch.context_lens)
+    host["block_tables"].copy_(batch.block_tables)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            sess.step_from_host(host, status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(float(i))
+            e2e_ev[i][0].record(stream)
+            sess.step_from_host(host, status=status, stream=stream)
+            e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    ref_out = out.cpu()
+    if not torch.equal(host["out"], ref_out):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
+
+    dbytes = decode_bytes(ctx, B, H, D, bs)
+    sbytes = dbytes + write_bytes(int(batch.slot_mapping.numel()), H, D)
+    res = {
+        "step_ms": total_ms / K, "decode_ms": statistics.mean(dec_ms),
+        "decode_ms_median": statistics.median(dec_ms), "write_ms": statistics.mean(wr_ms),
+        "e2e_ms": e2e_ms / K, "step_bytes": sbytes, "decode_bytes": dbytes,
+        "tokens": int(ctx.sum()), "clocks": clocks.summary(), "partition_tokens": pt,
+        "num_parts": n_parts, "launches": launches_per_step * K,
+        "h2d": sess.h2d_bytes(), "d2h": sess.d2h_bytes(),
+        "batch": batch,
+    }
+    return res
+
+
+def cpu_baseline(batch, budget_s):
+    """Time the fp64 oracle (single thread) on a bounded sample of the
+    workload: the cache write of the new tokens, then decode of the first
+    sequences whose estimated cost fits ``budget_s``."""
+    import oracle
+    kc = batch.k_cache.cpu().numpy()
+    vc = batch.v_cache.cpu().numpy()
+    q = batch.q.cpu().numpy()
+    bt = batch.block_tables.cpu().numpy()
+    ctx = batch.context_lens.cpu().numpy()
+    kn, vn = batch.k_new.cpu().numpy(), batch.v_new.cpu().numpy()
+    sm = batch.slot_mapping.cpu().numpy()
+    H, D, bs = batch.H, batch.D, batch.block_size
+    # calibrate: one sequence
+    t0 = time.perf_counter()
+    oracle.decode(q[:1], kc, vc, bt[:1], ctx[:1], batch.scale)
+    per_token = (time.perf_counter() - t0) / max(int(ctx[0]), 1)
+    n = 1
+    while n < len(ctx) and per_token * ctx[:n + 1].sum() < budget_s:
+        n += 1
+    t0 = time.perf_counter()
+    kc2, vc2 = oracle.kv_cache_write(kn, vn, sm, kc, vc)
+    oracle.decode(q[:n], kc2, vc2, bt[:n], ctx[:n], batch.scale)
+    dt = time.perf_counter() - t0
+    byts = decode_bytes(ctx[:n], n, H, D, bs) + write_bytes(len(sm), H, D)
+    return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"cache write of {len(sm)} tokens + decode of the first {n} of "
+                      f"{len(ctx)} sequences ({int(ctx[:n].sum())} keys x {H} heads), fp64, "
+                      "single thread"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import oracle
+    batch = make_workload("cpu", seed=1)
+    H, D, bs = batch.H, batch.D, batch.block_size
+    kc = batch.k_cache.numpy()
+    vc = batch.v_cache.numpy()
+    q, bt, ctx = batch.q.numpy(), batch.block_tables.numpy(), batch.context_lens.numpy()
+    kn, vn, sm = batch.k_new.numpy(), batch.v_new.numpy(), batch.slot_mapping.numpy()
+    budget = args.reference_budget_s / max(args.steps + args.warmup, 1)
+    t0 = time.perf_counter()
+    oracle.decode(q[:1], kc, vc, bt[:1], ctx[:1], batch.scale)
+    per_token = (time.perf_counter() - t0) / int(ctx[0])
+    n = 1
+    while n < len(ctx) and per_token * ctx[:n + 1].sum() < budget:
+        n += 1
+
+    def one():
+        kc2, vc2 = oracle.kv_cache_write(kn, vn, sm, kc, vc)
+        oracle.decode(q[:n], kc2, vc2, bt[:n], ctx[:n], batch.scale)
+
+    for _ in range(args.warmup):
+        one()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        ts.append(time.perf_counter() - t0)
+    byts = decode_bytes(ctx[:n], n, H, D, bs) + write_bytes(len(sm), H, D)
+    secs = sum(ts)
+    value = byts * args.steps / secs / 1e9
+    sample = (f"cache write of {len(sm)} tokens + decode of the first {n} of {len(ctx)} "
+              f"sequences ({int(ctx[:n].sum())} keys x {H} heads) per step, fp64, one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(batch, None, "n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_config(batch, pt, l2):
+    ctx = batch.context_lens.cpu().numpy()
+    return {"workload": "llama13b_decode_b38: 38 seqs x 40 heads x head_dim 128, block_size "
+                        "16, context_lens U[128,2048] (seed 1), pool 1.2x need, randomly "
+                        "permuted blocks; step = kv_cache_write of 38 new tokens + pa_decode",
+            "B": int(batch.B), "H": int(batch.H), "head_dim": int(batch.D),
+            "block_size": int(batch.block_size), "num_blocks": int(batch.num_blocks),
+            "sum_context_len": int(ctx.sum()), "partition_tokens": pt, "l2": l2}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    K = args.steps
+    total_s = res["step_ms"] * K / 1e3
+    step_bytes = res["step_bytes"]
+    dec_s = res["decode_ms"] / 1e3
+    if world > 1:
+        t = torch.tensor([total_s, res["e2e_ms"] * K / 1e3], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s, e2e_s = t.tolist()
+        b = torch.tensor([float(step_bytes)], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(b)
+        all_bytes = b.item()
+    else:
+        e2e_s = res["e2e_ms"] * K / 1e3
+        all_bytes = float(step_bytes)
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    value = all_bytes * K / total_s / 1e9
+    achieved = res["decode_bytes"] / dec_s / 1e9
+    key = src_hash("decode.cu")
+    traffic = DECODE_TRAFFIC.get(key)
+    batch = res["batch"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_s / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 storage, f32 accumulate",
+        "data": "synthetic (seeded fp16 N(0,1))",
+        "config": workload_config(batch, res["partition_tokens"],
+                                  "flushed before every timed step (512 MB write, untimed)"),
+        "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
+        f"frac_of_{peak_kind}_hbm": value / peak,
+        "attended_tokens_per_s": res["tokens"] * world / (dec_s),
+        "decode_ms": res["decode_ms"], "decode_ms_median": res["decode_ms_median"],
+        "write_ms": res["write_ms"],
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (partition + combine kernels)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes": res["decode_bytes"]},
+        "e2e": {"value": all_bytes * K / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": e2e_s / K * 1e3},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch, args.cpu_budget_s)
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: attention over a paged KV cache on one
+ * NVIDIA GB300 (sm_103a), plus the two cache-maintenance copies.
+ *
+ * The problem statement these calls implement comes from three pages:
+ *  - blog "PagedAttention origin and evolution" (PagedAttention的起源与演进),
+ *    sec. 3.2.1 (K and V pools of shape [num_blocks, block_size, num_heads,
+ *    head_dim], fp16) and sec. 3.2.2 (forward pass: per request, gather K/V
+ *    through block_tables[batch, max_num_blocks], cut to context_lens,
+ *    Q K^T / sqrt(head_dim), softmax, weighted sum of V);
+ *  - tutorial chapter "4. PagedAttention机制：vLLM的核心创新", sections
+ *    "PagedAttention的核心思想" (fixed-size blocks of 16 or 32 tokens, not
+ *    contiguous, mapped by a Block Table), "Block管理策略" (blocks taken and
+ *    returned through a free list as the cache grows) and
+ *    "PagedAttention的注意力计算" (per logical block: physical =
+ *    block_table[logical], score every token, softmax, weighted V);
+ *  - study notes "DataWhale组队学习笔记--llm-algo-leetcode(五)", sections
+ *    "3. PagedAttention 的工作机制" (the lookup is transparent to the model)
+ *    and "4. PagedAttention 带来的核心红利" (sequences sharing a prompt point
+ *    at the same physical blocks; a block is copied when one of them writes).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - fp16 data (pa_half) is IEEE binary16, passed as raw 16-bit patterns.
+ *  - Every pointer argument except the host-side scalars is a DEVICE pointer
+ *    of the current CUDA device, row-major and contiguous.  The caller owns
+ *    all memory; the library allocates nothing and never synchronises.
+ *  - Every call is asynchronous on `stream` (0 = the legacy default stream).
+ *  - Argument errors are reported synchronously, before anything is
+ *    launched: PA_ERR_INVALID for a bad pointer, size or alignment,
+ *    PA_ERR_UNSUPPORTED for a head_dim / block_size pair with no kernel,
+ *    PA_ERR_WORKSPACE for a workspace that is too small, PA_ERR_CUDA when a
+ *    launch fails (pa_last_cuda_error() then holds the cudaError_t value).
+ *  - Errors in device-resident data (a block id outside [0, num_blocks), a
+ *    context length out of range, a slot outside the pool, a copy pair out
+ *    of range) are detected by the kernels: the affected work is skipped or
+ *    clamped, never read or written out of bounds, and the PA_DEV_* bit is
+ *    OR-ed into `*status` when `status` (a device int32) is not NULL.  The
+ *    caller zeroes *status before the call and reads it afterwards.
+ *  - Buffers that a call reads must not be written by the same call
+ *    (no aliasing between inputs and outputs).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_half;               /* IEEE binary16 bit pattern */
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,
+    PA_ERR_UNSUPPORTED = 2,
+    PA_ERR_WORKSPACE = 3,
+    PA_ERR_CUDA = 4
+} pa_status;
+
+/* Bits OR-ed into the device status word. */
+#define PA_DEV_BAD_BLOCK_ID 0x1   /* a needed block-table entry is outside [0, num_blocks) */
+#define PA_DEV_BAD_CONTEXT 0x2    /* context length < 0, > max_context_len or > table capacity */
+#define PA_DEV_BAD_SLOT 0x4       /* a slot >= num_blocks * block_size */
+#define PA_DEV_BAD_PAIR 0x8       /* a copy pair outside [0, num_blocks) */
+#define PA_DEV_TIMEOUT 0x10       /* a bounded wait inside a kernel gave up */
+
+/* Human-readable name of a status code (static storage). */
+const char *pa_status_string(pa_status s);
+
+/* cudaError_t value behind the last PA_ERR_CUDA returned on this thread. */
+int pa_last_cuda_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Decode attention (one query token per sequence).
+ *
+ * Definition (blog sec. 3.2.2, tutorial "PagedAttention的注意力计算"): for each
+ * sequence b and head h, with n = context_lens[b] and key j stored in
+ * physical block block_tables[b][j / block_size], token slot j % block_size,
+ *     s_j   = scale * sum_d q[b,h,d] * k_cache[blk(j), j % bs, h, d]
+ *     p_j   = exp(s_j - max_k s_k) / sum_k exp(s_k - max_k s_k)
+ *     out[b,h,:] = sum_j p_j * v_cache[blk(j), j % bs, h, :]
+ * for j in [0, n).  n == 0 gives a zero row.  Only the first
+ * ceil(n / block_size) entries of a table row are read; later entries may
+ * hold anything (conventionally -1).
+ *
+ * q            [B, H, D] fp16
+ * k_cache      [num_blocks, block_size, H, D] fp16 (v_cache alike)
+ * block_tables [B, max_blocks_per_seq] int32
+ * context_lens [B] int32, each in [0, min(max_context_len,
+ *              max_blocks_per_seq * block_size)]
+ * out          [B, H, D] fp16, written with round-to-nearest-even from an
+ *              fp32 accumulation
+ * D in {64, 128}; block_size in {4, 8, 16, 32}; q, k_cache, v_cache and out
+ * 16-byte aligned.
+ *
+ * Long contexts are split into partitions of `partition_tokens` keys (a
+ * multiple of block_size, at most 32 blocks; 0 picks one from B, H and
+ * max_context_len); each partition's running max, normaliser and
+ * unnormalised output go to `workspace` and a second kernel merges them by
+ * log-sum-exp.  max_context_len is a host-side bound on every
+ * context_lens[b] so the split plan never reads device memory.
+ * workspace: device memory of at least
+ * pa_decode_workspace_size(B, H, D, block_size, max_context_len,
+ * partition_tokens) bytes, 16-byte aligned, owned by the caller, contents
+ * need not be initialised; may be NULL when that size is 0.
+ * ------------------------------------------------------------------------- */
+int pa_decode_partition_tokens(int B, int H, int block_size, int max_context_len);
+
+size_t pa_decode_workspace_size(int B, int H, int D, int block_size,
+                                int max_context_len, int partition_tokens);
+
+pa_status pa_decode(const pa_half *q, const pa_half *k_cache,
+                    const pa_half *v_cache, const int32_t *block_tables,
+                    const int32_t *context_lens, int B, int H, int D,
+                    int block_size, int num_blocks, int max_blocks_per_seq,
+                    int max_context_len, int partition_tokens, float scale,
+                    pa_half *out, void *workspace, size_t workspace_bytes,
+                    int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Chunked prefill attention (Lq new query tokens per sequence).
+ *
+ * The Lq queries of sequence b are its last Lq positions: query i sits at
+ * position n - Lq + i, n = context_lens[b] (which counts the chunk, whose
+ * K/V must already be in the cache), and attends to keys
+ * 0 .. n - Lq + i (causal mask aligned to the end of the context; with
+ * Lq == n this is the lower-triangular mask of the blog's sec. 3.2.2, with
+ * Lq == 1 it is decode).  Same per-row arithmetic as pa_decode.
+ *
+ * q   [B, H, Lq, D] fp16 (the blog's [batch, heads, seq_len, head_dim])
+ * out [B, H, Lq, D] fp16
+ * context_lens[b] in [Lq, max_blocks_per_seq * block_size].
+ * D == 128 and block_size in {16, 32} run on the tcgen05 tensor-core kernel;
+ * other supported (D, block_size) pairs return PA_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+pa_status pa_prefill_chunk(const pa_half *q, const pa_half *k_cache,
+                           const pa_half *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int B, int H, int Lq,
+                           int D, int block_size, int num_blocks,
+                           int max_blocks_per_seq, float scale, pa_half *out,
+                           int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Cache write (scatter new tokens' K/V into their slots).
+ *
+ * With the caches viewed as [num_blocks * block_size, H, D], for each token
+ * t with slot_mapping[t] >= 0:  k_cache[slot] = k[t], v_cache[slot] = v[t]
+ * (bit-exact copies).  slot = physical_block * block_size + offset, the
+ * address a sequence's block table gives its position (tutorial, "Block管理
+ * 策略": the cache grows into newly mapped blocks).  Negative slots are
+ * padding and are skipped.  Two tokens with the same slot: undefined which
+ * one lands.
+ *
+ * k, v          [T, H, D] fp16
+ * slot_mapping  [T] int64
+ * k_cache, v_cache as for pa_decode, written in place.
+ * ------------------------------------------------------------------------- */
+pa_status pa_kv_cache_write(const pa_half *k, const pa_half *v,
+                            const int64_t *slot_mapping, int T, int H, int D,
+                            int block_size, int num_blocks, pa_half *k_cache,
+                            pa_half *v_cache, int32_t *status,
+                            pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Block copy (copy-on-write of shared blocks; study notes sec. 4).
+ *
+ * For each pair i: physical block pairs[i][1] of k_cache and of v_cache
+ * becomes a bit-exact copy of block pairs[i][0] (all block_size * H * D
+ * values).  Destinations must be distinct and no destination may be the
+ * source of another pair in the same call (otherwise the result is
+ * undefined); src == dst is a no-op.
+ *
+ * pairs [N, 2] int64 (src, dst).
+ * ------------------------------------------------------------------------- */
+pa_status pa_block_copy(pa_half *k_cache, pa_half *v_cache,
+                        const int64_t *pairs, int N, int H, int D,
+                        int block_size, int num_blocks, int32_t *status,
+                        pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,210 @@
+"""ctypes binding of libpagedkv (include/pagedkv.h).
+
+Argument marshalling only: every step of the path runs in the library's
+CUDA kernels.  PyTorch supplies device memory and streams.  If the compiled
+library is missing the first call raises; there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_DEV_BAD_BLOCK_ID = 0x1
+PA_DEV_BAD_CONTEXT = 0x2
+PA_DEV_BAD_SLOT = 0x4
+PA_DEV_BAD_PAIR = 0x8
+PA_DEV_TIMEOUT = 0x10
+
+# Every symbol include/pagedkv.h declares.
+EXPORTS = (
+    "pa_status_string", "pa_last_cuda_error", "pa_version",
+    "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
+    "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
+)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+def _bind(lib):
+    lib.pa_status_string.argtypes = [_I]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_cuda_error.argtypes = []
+    lib.pa_last_cuda_error.restype = _I
+    lib.pa_version.argtypes = []
+    lib.pa_version.restype = _I
+    lib.pa_decode_partition_tokens.argtypes = [_I, _I, _I, _I]
+    lib.pa_decode_partition_tokens.restype = _I
+    lib.pa_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+    lib.pa_decode_workspace_size.restype = _SZ
+    lib.pa_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                              ctypes.c_float, _P, _P, _SZ, _P, _P]
+    lib.pa_decode.restype = _I
+    lib.pa_prefill_chunk.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _P, _P, _P]
+    lib.pa_prefill_chunk.restype = _I
+    lib.pa_kv_cache_write.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]
+    lib.pa_kv_cache_write.restype = _I
+    lib.pa_block_copy.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
+    lib.pa_block_copy.restype = _I
+    return lib
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libpagedkv.so not found at {LIB_PATH}: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(code):
+    return lib().pa_status_string(int(code)).decode()
+
+
+def _check(rc, what):
+    if rc != PA_OK:
+        err = PagedKVError(rc, what)
+        if rc == PA_ERR_CUDA:
+            err.cuda_error = lib().pa_last_cuda_error()
+        raise err
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def pa_decode_partition_tokens(B, H, block_size, max_context_len):
+    return lib().pa_decode_partition_tokens(B, H, block_size, max_context_len)
+
+
+def pa_decode_workspace_size(B, H, D, block_size, max_context_len, partition_tokens=0):
+    return lib().pa_decode_workspace_size(B, H, D, block_size, max_context_len,
+                                          partition_tokens)
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+              out=None, partition_tokens=0, workspace=None, status=None, stream=None):
+    """Paged decode attention.  q [B,H,D] fp16; caches [NB,bs,H,D] fp16;
+    block_tables [B,max_blocks] int32; context_lens [B] int32;
+    ``max_context_len`` is a host-side upper bound on context_lens.
+    Returns ``out`` [B,H,D] fp16 (allocated when not given)."""
+    _need(q, torch.float16, "q", 3)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables/context_lens batch mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float16, "out", 3)
+    ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
+                                        partition_tokens)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                         _ptr(context_lens), B, H, D, bs, NB, block_tables.shape[1],
+                         int(max_context_len), int(partition_tokens), float(scale), _ptr(out),
+                         _ptr(workspace), ws_len, _ptr(status), _stream(stream, q.device))
+    _check(rc, "pa_decode")
+    return out
+
+
+def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                     status=None, stream=None):
+    """Chunked prefill attention.  q [B,H,Lq,D] fp16 are the last Lq positions
+    of each sequence (end-aligned causal mask).  Returns out [B,H,Lq,D]."""
+    _need(q, torch.float16, "q", 4)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, H, Lq, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float16, "out", 4)
+    rc = lib().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), B, H, Lq, D, bs, NB,
+                                block_tables.shape[1], float(scale), _ptr(out), _ptr(status),
+                                _stream(stream, q.device))
+    _check(rc, "pa_prefill_chunk")
+    return out
+
+
+def pa_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, status=None, stream=None):
+    """Scatter k/v [T,H,D] fp16 into the caches at slot_mapping [T] int64."""
+    _need(k, torch.float16, "k", 3)
+    _need(v, torch.float16, "v", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    T, H, D = k.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    if v.shape != k.shape or slot_mapping.shape[0] != T:
+        raise ValueError("k/v/slot_mapping shape mismatch")
+    if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
+    rc = lib().pa_kv_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, bs, NB,
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(status),
+                                 _stream(stream, k.device))
+    _check(rc, "pa_kv_cache_write")
+
+
+def pa_block_copy(k_cache, v_cache, pairs, status=None, stream=None):
+    """Copy whole physical blocks: pairs [N,2] int64 (src, dst)."""
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(pairs, torch.int64, "pairs", 2)
+    NB, bs, H, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or pairs.shape[1] != 2:
+        raise ValueError("bad k_cache/v_cache/pairs shapes")
+    rc = lib().pa_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], H, D,
+                             bs, NB, _ptr(status), _stream(stream, k_cache.device))
+    _check(rc, "pa_block_copy")

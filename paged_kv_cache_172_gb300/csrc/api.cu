@@ -1,0 +1,253 @@
+// api.cu -- the extern "C" entry points of libpagedkv (declared in
+// include/pagedkv.h): argument validation, the decode partition plan, TMA
+// tensor-map encoding, and the launches.  No entry point allocates memory or
+// synchronises.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "pk_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+pa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool block_size_ok(int bs) { return bs == 4 || bs == 8 || bs == 16 || bs == 32; }
+
+// Largest pool the kernels address with 32-bit row coordinates.
+bool pool_ok(int num_blocks, int block_size, int H, int D) {
+  if (num_blocks <= 0 || H <= 0 || D <= 0) return false;
+  const long long rows = (long long)num_blocks * block_size;
+  if (rows >= (1LL << 31)) return false;
+  const long long elems = rows * H * D;
+  return elems / rows == (long long)H * D && elems < (1LL << 46);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+namespace pk {
+
+cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, int H, int D,
+                          int box_heads, int box_tokens) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace pk
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID: bad pointer, size or alignment";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: no kernel for this head_dim/block_size";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA launch error";
+  }
+  return "unknown pa_status";
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pa_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+int pa_decode_partition_tokens(int B, int H, int block_size, int max_context_len) {
+  if (B <= 0 || H <= 0 || !block_size_ok(block_size) || max_context_len <= 0) return block_size;
+  // Aim for at least ~8192 warp work items (152 SMs x 4-warp CTAs x several
+  // waves), without partitions shorter than 8 blocks or longer than 32.
+  const long long pairs = (long long)B * H;
+  const long long want_parts = (8192 + pairs - 1) / pairs;
+  long long tokens = (max_context_len + want_parts - 1) / want_parts;
+  const long long lo = 8LL * block_size, hi = 32LL * block_size;
+  if (tokens < lo) tokens = lo;
+  if (tokens > hi) tokens = hi;
+  tokens = (tokens + block_size - 1) / block_size * block_size;
+  return (int)tokens;
+}
+
+static int resolve_partition(int B, int H, int block_size, int max_context_len,
+                             int partition_tokens) {
+  return partition_tokens > 0
+             ? partition_tokens
+             : pa_decode_partition_tokens(B, H, block_size, max_context_len);
+}
+
+size_t pa_decode_workspace_size(int B, int H, int D, int block_size, int max_context_len,
+                                int partition_tokens) {
+  if (B <= 0 || H <= 0 || D <= 0 || !block_size_ok(block_size) || max_context_len <= 0) return 0;
+  const int pt = resolve_partition(B, H, block_size, max_context_len, partition_tokens);
+  if (pt <= 0) return 0;
+  const long long parts = (max_context_len + pt - 1) / pt;
+  if (parts <= 1) return 0;
+  return (size_t)B * H * parts * (size_t)(D + 2) * sizeof(float);
+}
+
+pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int B, int H, int D,
+                    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
+                    int partition_tokens, float scale, pa_half* out, void* workspace,
+                    size_t workspace_bytes, int32_t* status, pa_stream_t stream) {
+  if (B < 0 || H <= 0 || H > 65535 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
+      !isfinite(scale))
+    return PA_ERR_INVALID;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (B == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_INVALID;
+  if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
+    return PA_ERR_INVALID;
+  if (max_context_len == 0) max_context_len = 1;  // every row is empty: one partition
+  const int pt = resolve_partition(B, H, block_size, max_context_len, partition_tokens);
+  if (pt <= 0 || pt % block_size != 0 || pt > 32 * block_size) return PA_ERR_INVALID;
+  const long long parts = (max_context_len + pt - 1) / pt;
+  if (parts > 65535) return PA_ERR_INVALID;
+  const size_t need = pa_decode_workspace_size(B, H, D, block_size, max_context_len, pt);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(workspace)) return PA_ERR_INVALID;
+
+  const long long rows = (long long)num_blocks * block_size;
+  CUtensorMap kmap, vmap;
+  cudaError_t e = pk::make_pool_map(&kmap, k_cache, rows, H, D, 1, block_size);
+  if (e != cudaSuccess) return PA_ERR_INVALID;
+  e = pk::make_pool_map(&vmap, v_cache, rows, H, D, 1, block_size);
+  if (e != cudaSuccess) return PA_ERR_INVALID;
+
+  pk::DecodeArgs a;
+  a.q = reinterpret_cast<const __half*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  float* ws = reinterpret_cast<float*>(workspace);
+  a.ws_o = need ? ws : nullptr;
+  a.ws_ml = need ? ws + (size_t)B * H * parts * D : nullptr;
+  a.status = status;
+  a.B = B;
+  a.H = H;
+  a.D = D;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.part_tokens = pt;
+  a.num_parts = (int)parts;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  e = pk::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// chunked prefill
+// ---------------------------------------------------------------------------
+pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, int B, int H,
+                           int Lq, int D, int block_size, int num_blocks, int max_blocks_per_seq,
+                           float scale, pa_half* out, int32_t* status, pa_stream_t stream) {
+  if (B < 0 || H <= 0 || Lq < 0 || max_blocks_per_seq <= 0 || !isfinite(scale))
+    return PA_ERR_INVALID;
+  if (!pk::prefill_supported(D, block_size)) return PA_ERR_UNSUPPORTED;
+  if (B == 0 || Lq == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_INVALID;
+  if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  if ((long long)Lq > (long long)max_blocks_per_seq * block_size) return PA_ERR_INVALID;
+  pk::PrefillArgs a;
+  a.q = reinterpret_cast<const __half*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = reinterpret_cast<__half*>(out);
+  a.status = status;
+  a.B = B;
+  a.H = H;
+  a.Lq = Lq;
+  a.D = D;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  cudaError_t e = pk::launch_prefill(a, k_cache, v_cache, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return PA_ERR_INVALID;
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// cache write / block copy
+// ---------------------------------------------------------------------------
+pa_status pa_kv_cache_write(const pa_half* k, const pa_half* v, const int64_t* slot_mapping, int T,
+                            int H, int D, int block_size, int num_blocks, pa_half* k_cache,
+                            pa_half* v_cache, int32_t* status, pa_stream_t stream) {
+  if (T < 0 || H <= 0 || D <= 0) return PA_ERR_INVALID;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (T == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID;
+  if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  cudaError_t e = pk::launch_kv_cache_write(
+      reinterpret_cast<const __half*>(k), reinterpret_cast<const __half*>(v), slot_mapping, T, H,
+      D, (long long)num_blocks * block_size, reinterpret_cast<__half*>(k_cache),
+      reinterpret_cast<__half*>(v_cache), status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_block_copy(pa_half* k_cache, pa_half* v_cache, const int64_t* pairs, int N, int H,
+                        int D, int block_size, int num_blocks, int32_t* status,
+                        pa_stream_t stream) {
+  if (N < 0 || H <= 0 || D <= 0) return PA_ERR_INVALID;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (N == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs) return PA_ERR_INVALID;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+  if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  const long long block_elems = (long long)block_size * H * D;
+  for (int first = 0; first < N; first += 65535) {
+    const int n = N - first < 65535 ? N - first : 65535;
+    cudaError_t e = pk::launch_block_copy(
+        reinterpret_cast<__half*>(k_cache), reinterpret_cast<__half*>(v_cache),
+        pairs + 2LL * first, n, block_elems, num_blocks, status,
+        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,405 @@
+// decode.cu -- paged decode attention for sm_103a.
+//
+// Definition (blog "PagedAttention origin and evolution", sec. 3.2.2, and the
+// tutorial "4. PagedAttention机制：vLLM的核心创新", section
+// "PagedAttention的注意力计算"): one query per (sequence, head) attends to all
+// context_lens[b] keys, each key found through block_tables[b][j / bs].
+//
+// Design (GB300):
+//  * Work unit = one warp = one (sequence b, head h, partition of
+//    part_tokens keys).  A CTA holds WARPS warps for WARPS consecutive heads
+//    of the same (b, partition), so all its warps stream the same number of
+//    blocks.  Grid = (B, ceil(H / WARPS), num_parts) with b fastest: the
+//    sequences that share prompt blocks are scheduled together, so shared
+//    blocks are read from HBM once and served from L2 to the sharers.
+//  * Each warp runs its own NSTAGE-deep TMA pipeline: lane 0 issues one 3-D
+//    tensor load per block for K and one for V (box = block_size rows of one
+//    head, the rows being block_size tokens apart by H*D*2 bytes in the pool),
+//    completing on a per-stage mbarrier.  The block-table entries of the
+//    partition are loaded once, one per lane, so address generation never
+//    waits on a dependent global load.
+//  * Scores: lane l owns D/32 consecutive dims; every lane forms partial dot
+//    products for all block_size tokens of the block, then a transposing
+//    butterfly (offsets 16, 8, ...) halves the number of live values per step
+//    so that after log2(block_size) shuffle rounds each lane holds the full
+//    score of token lane / (32 / block_size): block_size + ... + 1 shuffles
+//    instead of 5 per token.
+//  * Online softmax in the log2 domain (scale * log2(e) folded into one
+//    multiply), fp32 accumulation of P V with the lane's D/32 dims.
+//  * A sequence that fits in one partition writes fp16 output directly;
+//    otherwise each partition writes (max, normaliser, unnormalised output)
+//    to the workspace and combine_kernel merges them by log-sum-exp.
+#include <math.h>
+
+#include "pk_common.cuh"
+#include "pk_internal.h"
+
+namespace pk {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int EPL>
+struct LaneVec;  // EPL fp16 values of one lane
+template <>
+struct LaneVec<4> {
+  uint2 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ void to_float(float* f) const {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+};
+template <>
+struct LaneVec<2> {
+  uint32_t raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ __forceinline__ void to_float(float* f) const {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+    f[0] = a.x; f[1] = a.y;
+  }
+};
+
+template <int EPL>
+__device__ __forceinline__ void store_half_row(__half* dst, const float* v) {
+  if constexpr (EPL == 4) {
+    __half2 a = __floats2half2_rn(v[0], v[1]);
+    __half2 b = __floats2half2_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+    __half2 a = __floats2half2_rn(v[0], v[1]);
+    *reinterpret_cast<__half2*>(dst) = a;
+  }
+}
+
+// Context length of sequence b clamped to what the launch can address.
+__device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool report) {
+  int ctx = a.context_lens[b];
+  const int cap = min(a.max_context_len, a.max_blocks * a.block_size);
+  if (ctx < 0 || ctx > cap) {
+    if (report) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  return ctx;
+}
+
+template <int D, int BS, int WARPS, int NSTAGE>
+struct PartitionCfg {
+  static constexpr int EPL = D / 32;                  // dims per lane
+  static constexpr int TILE_BYTES = BS * D * 2;       // one head's rows of one block
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
+  static constexpr int LANES_PER_TOKEN = 32 / BS;     // lanes sharing a score after the butterfly
+  static constexpr int SMEM_BYTES = WARPS * NSTAGE * STAGE_BYTES + WARPS * NSTAGE * 8;
+};
+
+template <int D, int BS, int WARPS, int NSTAGE>
+__global__ void __launch_bounds__(WARPS * 32)
+    partition_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE>;
+  constexpr int EPL = Cfg::EPL;
+  constexpr int LPT = Cfg::LANES_PER_TOKEN;
+  static_assert(BS >= 1 && BS <= 32 && (32 % BS) == 0, "block_size must divide 32");
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * WARPS + warp;
+  const int part = blockIdx.z;
+  if (h >= a.H) return;  // idle warp of a ragged head group (no CTA-wide sync below)
+
+  uint8_t* wbase = smem + warp * NSTAGE * Cfg::STAGE_BYTES;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + WARPS * NSTAGE * Cfg::STAGE_BYTES) + warp * NSTAGE;
+
+  const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
+  const int tok0 = part * a.part_tokens;
+  const size_t row_bh = (size_t)b * a.H + h;
+  if (tok0 >= ctx) {
+    if (part == 0) {  // empty sequence: zero row
+      float z[EPL] = {};
+      store_half_row<EPL>(a.out + row_bh * D + lane * EPL, z);
+    }
+    return;
+  }
+  const int tok1 = min(ctx, tok0 + a.part_tokens);
+  const int lb0 = tok0 / BS;
+  const int nblk = (tok1 - tok0 + BS - 1) / BS;  // <= 32 by construction of part_tokens
+
+  // Block-table entries of this partition, one per lane.
+  int phys = 0;
+  if (lane < nblk) {
+    phys = a.block_tables[(size_t)b * a.max_blocks + lb0 + lane];
+    if (phys < 0 || phys >= a.num_blocks) {
+      flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+      phys = a.num_blocks;  // entirely outside the tensor map: TMA fills zeros
+    }
+  }
+
+  // Query slice of this lane.
+  float qf[EPL];
+  {
+    LaneVec<EPL> qv;
+    qv.load(a.q + row_bh * D + lane * EPL);
+    qv.to_float(qf);
+  }
+
+  if (lane == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Prologue: fill the pipeline.
+  for (int i = 0; i < NSTAGE && i < nblk; ++i) {
+    const int pb = __shfl_sync(kFull, phys, i);
+    if (lane == 0) {
+      uint8_t* st = wbase + i * Cfg::STAGE_BYTES;
+      mbar_arrive_expect_tx(&bars[i], Cfg::STAGE_BYTES);
+      tma_load_3d(st, &kmap, 0, h, pb * BS, &bars[i]);
+      tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, pb * BS, &bars[i]);
+    }
+  }
+
+  float m = -INFINITY, l = 0.f;
+  float o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+
+  const int my_tok = lane / LPT;  // token whose score this lane holds after the butterfly
+  int i = 0;
+  for (; i < nblk; ++i) {
+    const int s = i % NSTAGE;
+    const uint32_t parity = (i / NSTAGE) & 1;
+    const bool got = mbar_wait(&bars[s], parity);
+    if (!__all_sync(kFull, got)) break;
+
+    const __half* ks = reinterpret_cast<const __half*>(wbase + s * Cfg::STAGE_BYTES);
+    const __half* vs = ks + BS * D;
+    const int valid = min(BS, tok1 - (lb0 + i) * BS);  // tokens of this block inside the partition
+
+    // Partial dot products of every token of the block.
+    float part_dot[BS];
+#pragma unroll
+    for (int t = 0; t < BS; ++t) {
+      LaneVec<EPL> kv;
+      kv.load(ks + t * D + lane * EPL);
+      float kf[EPL];
+      kv.to_float(kf);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+      part_dot[t] = acc;
+    }
+    // Transposing butterfly: after round r, lanes keep half of the tokens.
+#pragma unroll
+    for (int cnt = BS, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int k = 0; k < cnt / 2; ++k) {
+        const float send = upper ? part_dot[k] : part_dot[k + cnt / 2];
+        const float keep = upper ? part_dot[k + cnt / 2] : part_dot[k];
+        part_dot[k] = keep + __shfl_xor_sync(kFull, send, off);
+      }
+    }
+    // Remaining lanes of the same token hold disjoint dim ranges: sum them.
+#pragma unroll
+    for (int off = LPT / 2; off >= 1; off >>= 1)
+      part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
+
+    float sc = (my_tok < valid) ? part_dot[0] * a.scale_log2 : -INFINITY;
+    float mb = sc;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+    const float m_new = fmaxf(m, mb);
+    const float alpha = fast_exp2(m - m_new);
+    const float pr = (my_tok < valid) ? fast_exp2(sc - m_new) : 0.f;
+    float psum = pr;
+#pragma unroll
+    for (int off = LPT; off <= 16; off <<= 1) psum += __shfl_xor_sync(kFull, psum, off);
+    l = l * alpha + psum;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= alpha;
+#pragma unroll
+    for (int t = 0; t < BS; ++t) {
+      const float pt = __shfl_sync(kFull, pr, t * LPT);
+      if (t < valid) {
+        LaneVec<EPL> vv;
+        vv.load(vs + t * D + lane * EPL);
+        float vf[EPL];
+        vv.to_float(vf);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
+      }
+    }
+    m = m_new;
+
+    // Refill this stage with block i + NSTAGE.
+    __syncwarp();
+    const int nxt = i + NSTAGE;
+    if (nxt < nblk) {
+      const int pb = __shfl_sync(kFull, phys, nxt);
+      if (lane == 0) {
+        uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[s], Cfg::STAGE_BYTES);
+        tma_load_3d(st, &kmap, 0, h, pb * BS, &bars[s]);
+        tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, pb * BS, &bars[s]);
+      }
+    }
+  }
+
+  if (i < nblk) {
+    // A bounded wait gave up: report, drain what is still in flight (again
+    // bounded) so no copy lands after the CTA exits, and write nothing.
+    if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+    for (int j = i; j < nblk && j < i + NSTAGE; ++j) mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
+    return;
+  }
+
+  const int n_parts = (ctx + a.part_tokens - 1) / a.part_tokens;
+  if (n_parts == 1) {
+    const float inv = 1.f / l;
+    float r[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) r[e] = o[e] * inv;
+    store_half_row<EPL>(a.out + row_bh * D + lane * EPL, r);
+  } else {
+    const size_t row = row_bh * a.num_parts + part;
+    float* dst = a.ws_o + row * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+    }
+    if (lane == 0) *reinterpret_cast<float2*>(a.ws_ml + row * 2) = make_float2(m, l);
+  }
+}
+
+// Log-sum-exp merge of the partitions of one (b, h):
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s 2^(m_s - M) o_s / L.
+template <int D, int THREADS>
+__global__ void __launch_bounds__(THREADS) combine_kernel(const DecodeArgs a) {
+  constexpr int NW = THREADS / 32;
+  constexpr int EPL = D / 32;
+  const int b = blockIdx.x;
+  const int h = blockIdx.y;
+  const int ctx = checked_ctx(a, b, false);
+  const int n = (ctx + a.part_tokens - 1) / a.part_tokens;
+  if (n <= 1) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t row0 = ((size_t)b * a.H + h) * a.num_parts;
+
+  __shared__ float red[NW];
+  __shared__ float acc_s[NW][D];
+
+  float mx = -INFINITY;
+  for (int s = tid; s < n; s += THREADS) mx = fmaxf(mx, a.ws_ml[(row0 + s) * 2]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+
+  float lsum = 0.f;
+  for (int s = tid; s < n; s += THREADS) {
+    const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (row0 + s) * 2);
+    lsum += ml.y * fast_exp2(ml.x - M);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+  if (lane == 0) red[warp] = lsum;
+
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int s = warp; s < n; s += NW) {
+    const float w = fast_exp2(a.ws_ml[(row0 + s) * 2] - M);
+    const float* src = a.ws_o + (row0 + s) * D + lane * EPL;
+    float v[EPL];
+    if constexpr (EPL == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc_s[warp][lane * EPL + e] = acc[e];
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) L += red[w];
+  const float inv = 1.f / L;
+  for (int d = tid; d < D; d += THREADS) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) t += acc_s[w][d];
+    a.out[((size_t)b * a.H + h) * D + d] = __float2half_rn(t * inv);
+  }
+}
+
+template <int D, int BS>
+struct DecodeTuning {
+  static constexpr int WARPS = 4;
+  // Aim for ~24 KB of K+V in flight per warp, 2..8 stages.
+  static constexpr int STAGE = 2 * BS * D * 2;
+  static constexpr int RAW = 24576 / STAGE;
+  static constexpr int NSTAGE = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
+};
+
+template <int D, int BS>
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+  using T = DecodeTuning<D, BS>;
+  using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE>;
+  auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE>;
+  static bool attr_done = false;  // per-process; the attribute is per function
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts);
+  kern<<<grid, T::WARPS * 32, Cfg::SMEM_BYTES, stream>>>(kmap, vmap, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.num_parts > 1) {
+    combine_kernel<D, 256><<<dim3(a.B, a.H), 256, 0, stream>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+bool decode_supported(int D, int block_size) {
+  return (D == 64 || D == 128) &&
+         (block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+#define PK_CASE(DD, BB) \
+  if (a.D == DD && a.block_size == BB) return launch_decode_t<DD, BB>(a, kmap, vmap, stream);
+  PK_CASE(128, 16) PK_CASE(128, 32) PK_CASE(128, 8) PK_CASE(128, 4)
+  PK_CASE(64, 16) PK_CASE(64, 32) PK_CASE(64, 8) PK_CASE(64, 4)
+#undef PK_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pk

@@ -1,0 +1,59 @@
+// pk_internal.h -- declarations shared between the C-ABI layer and the kernel
+// translation units (host side only).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pk {
+
+struct DecodeArgs {
+  const __half* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __half* out;
+  float* ws_o;    // [B, H, num_parts, D] unnormalised partition outputs
+  float* ws_ml;   // [B, H, num_parts, 2] partition (max, normaliser), log2 domain
+  int32_t* status;
+  int B, H, D, block_size, num_blocks, max_blocks, max_context_len;
+  int part_tokens, num_parts;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Encodes the [num_blocks * block_size, H, D] view of a cache pool as a 3-D
+// TMA tensor map with a box of (D, box_heads, box_tokens).
+cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, int H, int D,
+                          int box_heads, int box_tokens);
+
+// Launch the partition kernel then the combine kernel on `stream`.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+bool decode_supported(int D, int block_size);
+
+cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
+                                  int H, int D, long long n_slots, __half* kc, __half* vc,
+                                  int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_block_copy(__half* kc, __half* vc, const int64_t* pairs, int N,
+                              long long block_elems, int num_blocks, int32_t* status,
+                              cudaStream_t stream);
+
+struct PrefillArgs {
+  const __half* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __half* out;
+  int32_t* status;
+  int B, H, Lq, D, block_size, num_blocks, max_blocks;
+  float scale_log2;
+};
+bool prefill_supported(int D, int block_size);
+cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                           cudaStream_t stream);
+
+}  // namespace pk
