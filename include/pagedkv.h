@@ -125,6 +125,41 @@ pa_status pa_decode(const pa_half *q, const pa_half *k_cache,
                     int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode attention with no workspace and no allocation.
+ *
+ * This entry point has no counterpart on the pages; it exists for callers
+ * that cannot allocate device memory for a call -- a host runtime that has
+ * handed the whole device heap to its own pool, a plugin inside another
+ * engine that forbids allocations outside that engine's allocator, or a
+ * latency-critical loop that cannot pay for cudaMalloc's implicit device
+ * synchronisation.  It computes exactly what pa_decode computes, with the
+ * same arguments minus the workspace: the split-KV partition scratch lives
+ * in a fixed device array inside the library (PA_DECODE_STATIC_SCRATCH_BYTES,
+ * held on every GPU that loads the library until the process exits).
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - A plan needing more scratch than the array holds, i.e.
+ *    pa_decode_workspace_size(...) > PA_DECODE_STATIC_SCRATCH_BYTES, is
+ *    refused with PA_ERR_WORKSPACE before anything is launched; a smaller
+ *    partition count (larger partition_tokens) or batch fits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.  A failed look-up returns
+ *    PA_ERR_CUDA.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *    the GPU (different streams without ordering) race on it: serialise them.
+ * ------------------------------------------------------------------------- */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+
+pa_status pa_decode_static(const pa_half *q, const pa_half *k_cache,
+                           const pa_half *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int B, int H, int D,
+                           int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len,
+                           int partition_tokens, float scale, pa_half *out,
+                           int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Chunked prefill attention (Lq new query tokens per sequence).
  *
  * The Lq queries of sequence b are its last Lq positions: query i sits at

@@ -23,8 +23,11 @@ PA_DEV_TIMEOUT = 0x10
 EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
-    "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
+    "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy", "pa_decode_static",
 )
+
+# Size of the fixed scratch array behind pa_decode_static (PA_DECODE_STATIC_SCRATCH_BYTES).
+PA_DECODE_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class PagedKVError(RuntimeError):
@@ -60,6 +63,9 @@ def _bind(lib):
     lib.pa_kv_cache_write.restype = _I
     lib.pa_block_copy.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
     lib.pa_block_copy.restype = _I
+    lib.pa_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _P, _P, _P]
+    lib.pa_decode_static.restype = _I
     return lib
 
 

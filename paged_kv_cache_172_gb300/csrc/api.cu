@@ -49,6 +49,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 namespace pk {
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, int H, int D,
                           int box_heads, int box_tokens) {
   auto fn = encode_fn();

@@ -12,6 +12,9 @@
 
 namespace pk {
 
+// Makes `e` the value pa_last_cuda_error() reports on this thread.
+void record_cuda_error(cudaError_t e);
+
 struct DecodeArgs {
   const __half* q;
   const int32_t* block_tables;
