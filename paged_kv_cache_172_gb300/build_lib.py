@@ -6,6 +6,7 @@ runtime into ``paged_kv_cache_172_gb300/libpagedkv.so``.  Objects go to
 ``paged_kv_cache_172_gb300/_build/``.  Rebuilds only what changed.
 """
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -36,10 +37,10 @@ def _headers_mtime():
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src, extra):
-    obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+def _compile(src, extra, obj_dir):
+    obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
     if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
-            and os.path.getmtime(obj) >= _headers_mtime() and not extra):
+            and os.path.getmtime(obj) >= _headers_mtime()):
         return obj, None
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -48,11 +49,19 @@ def _compile(src, extra):
     return obj, r.stderr if "warning" in r.stderr.lower() else None
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), out=None) -> str:
+    """Compile and link.  ``extra_flags`` (e.g. -D tuning macros) build a
+    variant with its own object directory; ``out`` names its library path."""
+    extra_flags = tuple(extra_flags)
+    lib = out or LIB
+    obj_dir = OBJ_DIR
+    if extra_flags:
+        tag = hashlib.sha256(" ".join(extra_flags).encode()).hexdigest()[:10]
+        obj_dir = os.path.join(OBJ_DIR, "variant_" + tag)
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, list(extra_flags)), srcs))
+        results = list(ex.map(lambda s: _compile(s, list(extra_flags), obj_dir), srcs))
     errors = [msg for _, msg in results if msg and "error" in msg.lower()]
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
@@ -61,16 +70,16 @@ def build(verbose: bool = False, extra_flags=()) -> str:
             if msg:
                 print(msg, file=sys.stderr)
     objs = [o for o, _ in results]
-    if (os.path.exists(LIB) and not extra_flags
-            and all(os.path.getmtime(LIB) >= os.path.getmtime(o) for o in objs)):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+    if (os.path.exists(lib)
+            and all(os.path.getmtime(lib) >= os.path.getmtime(o) for o in objs)):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n$ {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     kv_cache_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                           const int64_t* __restrict__ slots, long long row_vecs, long long n_slots,
                           uint4* __restrict__ kc, uint4* __restrict__ vc, int32_t* status) {
+  pdl_launch_dependents();  // a following decode may be scheduled; it waits for this grid
   const int t = blockIdx.x;
   const long long slot = slots[t];
   if (slot < 0) return;  // padding token

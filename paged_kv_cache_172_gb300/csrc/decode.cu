@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int b = blockIdx.x;
   const int h = blockIdx.y * WARPS + warp;
   const int part = blockIdx.z;
+  pdl_wait();            // inputs may come from the previous kernel on the stream
   if (h >= a.H) return;  // idle warp of a ragged head group (no CTA-wide sync below)
 
   uint8_t* wbase = smem + warp * NSTAGE * Cfg::STAGE_BYTES;
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
 
+  pdl_launch_dependents();  // the combine kernel may be scheduled now
   if (i < nblk) {
     // A bounded wait gave up: report, drain what is still in flight (again
     // bounded) so no copy lands after the CTA exits, and write nothing.
@@ -284,82 +286,122 @@ __global__ void __launch_bounds__(WARPS * 32)
 
 // Log-sum-exp merge of the partitions of one (b, h):
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s 2^(m_s - M) o_s / L.
-template <int D, int THREADS>
-__global__ void __launch_bounds__(THREADS) combine_kernel(const DecodeArgs a) {
-  constexpr int NW = THREADS / 32;
+// One CTA of W = blockDim.x / 32 warps per (b, h); warp w takes partitions
+// w, w + W, ...; lane l owns dims [l * D/32, (l+1) * D/32).  W grows with
+// the partition count so a 1M-token context (thousands of partitions) still
+// keeps many loads in flight; W == 1 for short contexts needs no CTA sync.
+constexpr int kMaxCombineWarps = 16;
+
+template <int D>
+__global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
+  pdl_wait();  // partitions come from the partition kernel just before
   const int b = blockIdx.x;
   const int h = blockIdx.y;
   const int ctx = checked_ctx(a, b, false);
   const int n = (ctx + a.part_tokens - 1) / a.part_tokens;
   if (n <= 1) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int W = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row0 = ((size_t)b * a.H + h) * a.num_parts;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row0;
 
-  __shared__ float red[NW];
-  __shared__ float acc_s[NW][D];
+  __shared__ float red_m[kMaxCombineWarps];
+  __shared__ float red_l[kMaxCombineWarps];
+  __shared__ float red_o[kMaxCombineWarps][D];
 
   float mx = -INFINITY;
-  for (int s = tid; s < n; s += THREADS) mx = fmaxf(mx, a.ws_ml[(row0 + s) * 2]);
+  for (int s = threadIdx.x; s < n; s += blockDim.x) mx = fmaxf(mx, ml[s].x);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  float M = red[0];
-#pragma unroll
-  for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-
-  float lsum = 0.f;
-  for (int s = tid; s < n; s += THREADS) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (row0 + s) * 2);
-    lsum += ml.y * fast_exp2(ml.x - M);
+  if (W > 1) {
+    if (lane == 0) red_m[warp] = mx;
+    __syncthreads();
+    mx = red_m[0];
+    for (int w = 1; w < W; ++w) mx = fmaxf(mx, red_m[w]);
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-  if (lane == 0) red[warp] = lsum;
 
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  float lsum = 0.f;
 #pragma unroll 4
-  for (int s = warp; s < n; s += NW) {
-    const float w = fast_exp2(a.ws_ml[(row0 + s) * 2] - M);
+  for (int s = warp; s < n; s += W) {
+    const float2 p = ml[s];
+    const float w = fast_exp2(p.x - mx);
+    lsum = fmaf(p.y, w, lsum);
     const float* src = a.ws_o + (row0 + s) * D + lane * EPL;
-    float v[EPL];
     if constexpr (EPL == 4) {
       const float4 t = *reinterpret_cast<const float4*>(src);
-      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+      acc[0] = fmaf(w, t.x, acc[0]); acc[1] = fmaf(w, t.y, acc[1]);
+      acc[2] = fmaf(w, t.z, acc[2]); acc[3] = fmaf(w, t.w, acc[3]);
     } else {
       const float2 t = *reinterpret_cast<const float2*>(src);
-      v[0] = t.x; v[1] = t.y;
+      acc[0] = fmaf(w, t.x, acc[0]); acc[1] = fmaf(w, t.y, acc[1]);
     }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
   }
+  if (W > 1) {
+    if (lane == 0) red_l[warp] = lsum;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) acc_s[warp][lane * EPL + e] = acc[e];
-  __syncthreads();
-  float L = 0.f;
+    for (int e = 0; e < EPL; ++e) red_o[warp][lane * EPL + e] = acc[e];
+    __syncthreads();
+    if (warp != 0) return;
+    lsum = 0.f;
+    for (int w = 0; w < W; ++w) lsum += red_l[w];
 #pragma unroll
-  for (int w = 0; w < NW; ++w) L += red[w];
-  const float inv = 1.f / L;
-  for (int d = tid; d < D; d += THREADS) {
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) t += acc_s[w][d];
-    a.out[((size_t)b * a.H + h) * D + d] = __float2half_rn(t * inv);
+    for (int e = 0; e < EPL; ++e) {
+      float t = 0.f;
+      for (int w = 0; w < W; ++w) t += red_o[w][lane * EPL + e];
+      acc[e] = t;
+    }
   }
+  const float inv = 1.f / lsum;
+  float r[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = acc[e] * inv;
+  store_half_row<EPL>(a.out + ((size_t)b * a.H + h) * D + lane * EPL, r);
 }
+
+// Launch shape: WARPS heads per CTA, each warp with ~PK_DECODE_STAGE_BYTES of
+// K+V in flight (2..8 stages).  Both can be overridden at compile time.
+#ifndef PK_DECODE_WARPS
+#define PK_DECODE_WARPS 4
+#endif
+#ifndef PK_DECODE_INFLIGHT_BYTES
+#define PK_DECODE_INFLIGHT_BYTES 16384
+#endif
 
 template <int D, int BS>
 struct DecodeTuning {
-  static constexpr int WARPS = 4;
-  // Aim for ~24 KB of K+V in flight per warp, 2..8 stages.
+  static constexpr int WARPS = PK_DECODE_WARPS;
   static constexpr int STAGE = 2 * BS * D * 2;
-  static constexpr int RAW = 24576 / STAGE;
+#ifdef PK_DECODE_NSTAGE
+  static constexpr int NSTAGE = PK_DECODE_NSTAGE;
+#else
+  static constexpr int RAW = PK_DECODE_INFLIGHT_BYTES / STAGE;
   static constexpr int NSTAGE = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
+#endif
 };
+
+// Programmatic stream serialisation: the kernel may be scheduled before its
+// predecessor on the stream finishes; it calls griddepcontrol.wait before
+// touching any input, so ordering is preserved while the launch latency hides
+// behind the predecessor's tail.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 template <int D, int BS>
 cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -367,7 +409,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
   using T = DecodeTuning<D, BS>;
   using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE>;
   auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE>;
-  static bool attr_done = false;  // per-process; the attribute is per function
+  static bool attr_done = false;  // per process: the attribute belongs to the function
   if (!attr_done) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
@@ -375,12 +417,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
     attr_done = true;
   }
   dim3 grid(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts);
-  kern<<<grid, T::WARPS * 32, Cfg::SMEM_BYTES, stream>>>(kmap, vmap, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, kmap,
+                             vmap, a);
   if (e != cudaSuccess) return e;
   if (a.num_parts > 1) {
-    combine_kernel<D, 256><<<dim3(a.B, a.H), 256, 0, stream>>>(a);
-    e = cudaGetLastError();
+    int w = a.num_parts / 8;
+    w = w < 1 ? 1 : (w > kMaxCombineWarps ? kMaxCombineWarps : w);
+    e = launch_pdl(combine_kernel<D>, dim3(a.B, a.H), dim3(32 * w), 0, stream, a);
   }
   return e;
 }

@@ -112,6 +112,16 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+// Wait until every grid this one depends on has completed and its memory is
+// visible (a no-op when the launch was not programmatic).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next programmatically launched grid on the stream to be scheduled.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- misc --------------------------------------------------------------------
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 

@@ -33,6 +33,13 @@ struct DecodeArgs {
 cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, int H, int D,
                           int box_heads, int box_tokens);
 
+// General 3-D tiled tensor map over fp16 data: dims innermost first, byte
+// strides of dims 1 and 2, box extents; swizzle128 selects the 128-byte
+// shared-memory swizzle (the inner box must then be 64 fp16 = 128 bytes).
+cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long long dims[3],
+                        const unsigned long long strides[2], const unsigned box[3],
+                        bool swizzle128);
+
 // Launch the partition kernel then the combine kernel on `stream`.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);

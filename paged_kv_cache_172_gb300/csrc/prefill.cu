@@ -1,14 +1,425 @@
-// prefill.cu -- chunked prefill attention (tcgen05 tensor-core kernel).
-// Placeholder until the tensor-core kernel lands: reports "unsupported".
+// prefill.cu -- chunked prefill attention over a paged KV cache on the sm_103a
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Definition (blog "PagedAttention origin and evolution", sec. 3.2.2: per
+// request gather K/V through the block table, Q K^T / sqrt(d), causal mask,
+// softmax, P V; the mask is read as aligned to the END of the context, so the
+// Lq chunk queries sit at positions n-Lq .. n-1 and query i sees keys
+// 0 .. n-Lq+i).
+//
+// One CTA = 128 queries of one (sequence, head); it walks the visible keys in
+// tiles of 128 (8 blocks of 16 or 4 of 32 tokens):
+//   warp 0      TMA producer: Q once (2 x 64-dim slabs, 128-byte swizzle),
+//               then per key tile one box per (block, 64-dim slab) for K and
+//               for V, gathered through the block table, into a 4-stage ring;
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a double-buffered
+//               TMEM tile (8 x K=16 tcgen05.mma), then O += P_j V_j into the
+//               TMEM output accumulator once the softmax has written P_j;
+//               S_{j+1} is issued before waiting for P_j so the tensor core
+//               works on the next tile while the softmax runs;
+//   warps 2..5  softmax, one query row per thread (TMEM lane = row): load the
+//               row of S_j from TMEM, scale into the log2 domain, mask the
+//               diagonal tile, update the running max, write P_j (fp16) to a
+//               swizzled shared-memory tile for the next MMA.  The output
+//               accumulator is rescaled only when the max grows by more than
+//               2^8 (P then stays <= 256, exact in fp16 range), so most tiles
+//               skip the TMEM read-modify-write.  Epilogue: O / l -> fp16.
+// Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle):
+//   Q, K_j, P_j : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
+//                 the two 64-dim (or 64-key) halves 16 KB apart;
+//   V_j         : MN-major (dims contiguous): 8-key atoms 1024 B apart along
+//                 K, the two 64-dim halves 16 KB apart along N.
 #include "pk_common.cuh"
 #include "pk_internal.h"
+#include "pk_tcgen05.cuh"
 
 namespace pk {
 
-bool prefill_supported(int, int) { return false; }
+namespace {
 
-cudaError_t launch_prefill(const PrefillArgs&, const void*, const void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kTileM = 128;                  // queries per CTA
+constexpr int kTileN = 128;                  // keys per tile
+constexpr int kD = 128;                      // head dim
+constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
+constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
+constexpr int kStages = 4;                   // K/V ring (K and V tiles alternate)
+constexpr int kThreads = 192;
+constexpr int kTblWindow = 256;              // block-table entries staged in smem
+constexpr int kTmemCols = 512;               // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kColO = 256;
+
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kTileBytes;
+constexpr int kOffP = kOffKV + kStages * kTileBytes;
+constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
+constexpr int kOffTbl = (kOffTmemHolder + 4 + 15) / 16 * 16;
+constexpr int kSmemBytes = kOffTbl + kTblWindow * 4 + 1024;  // + alignment slack
+
+constexpr uint32_t kIdescS = tc::idesc_f16_f32(kTileM, kTileN, false, false);
+constexpr uint32_t kIdescO = tc::idesc_f16_f32(kTileM, kD, false, true);
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
+  // K step kk (16 elements = 32 B) inside the 64-element half kk / 4.
+  return tc::smem_desc(tile_addr + (kk >> 2) * kSlabBytes + (kk & 3) * 32, 16, 1024,
+                       tc::kSwizzle128B);
+}
+
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_addr, int kk) {
+  // keys 16*kk .. 16*kk+15: two 8-key atoms starting 2048 B * kk into the tile.
+  return tc::smem_desc(tile_addr + kk * 2048, kSlabBytes, 1024, tc::kSwizzle128B);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  constexpr int BPT = kTileN / BS;  // blocks per key tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sKV = smem + kOffKV;
+  uint8_t* sP = smem + kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
+  int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+
+  pdl_wait();  // inputs may come from the previous kernel on the stream
+  const int n = a.context_lens[b];
+  const int q0 = qt * kTileM;
+  const int rows = min(kTileM, a.Lq - q0);
+  const size_t out_row0 = ((size_t)b * a.H + h) * a.Lq + q0;
+  if (n < a.Lq || n > a.max_blocks * BS) {
+    if (threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * kD);
+    for (int i = threadIdx.x; i < rows * (kD / 8); i += kThreads) o4[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int pos0 = n - a.Lq + q0;        // sequence position of query row 0
+  const int last_key = pos0 + rows - 1;  // last key any valid row sees
+  const int n_tiles = last_key / kTileN + 1;
+  const int nblk_seq = (n + BS - 1) / BS;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+  int issued = 0;  // K/V tiles the producer issued into the ring
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int win = -kTblWindow;
+    if (lane == 0) {
+      const int bh = b * a.H + h;
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      tma_load_3d(sQ, &qmap, 0, q0, bh, q_full);
+      tma_load_3d(sQ + kSlabBytes, &qmap, 64, q0, bh, q_full);
+    }
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int lb0 = j * BPT;
+      if (lb0 + BPT > win + kTblWindow) {
+        win = lb0;
+        __syncwarp();
+        for (int i = lane; i < kTblWindow; i += 32) {
+          const int lb = win + i;
+          int phys = a.num_blocks;  // past the sequence: outside the map, TMA fills zeros
+          if (lb < nblk_seq) {
+            phys = a.block_tables[(size_t)b * a.max_blocks + lb];
+            if (phys < 0 || phys >= a.num_blocks) {
+              flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+              phys = a.num_blocks;
+            }
+          }
+          tbl_s[i] = phys;
+        }
+        __syncwarp();
+      }
+      for (int half = 0; half < 2 && ok; ++half) {  // K tile, then V tile
+        const int u = 2 * j + half;
+        const int st = u % kStages;
+        if (lane == 0) {
+          ok = mbar_wait(&kv_empty[st], ((u / kStages) & 1) ^ 1);
+          if (ok) {
+            uint8_t* dst = sKV + st * kTileBytes;
+            const CUtensorMap* map = half ? &vmap : &kmap;
+            mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
+#pragma unroll
+            for (int i = 0; i < BPT; ++i) {
+              const int row = tbl_s[lb0 - win + i] * BS;
+              tma_load_3d(dst + i * BS * 128, map, 0, h, row, &kv_full[st]);
+              tma_load_3d(dst + kSlabBytes + i * BS * 128, map, 64, h, row, &kv_full[st]);
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(kFull, ok, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t kv_addr = smem_u32(sKV);
+      const uint32_t p_addr = smem_u32(sP);
+      auto issue_s = [&](int j) -> bool {
+        const int u = 2 * j;
+        const int st = u % kStages;
+        if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t kb = kv_addr + st * kTileBytes;
+        const uint32_t d = tmem + (uint32_t)(j & 1) * kTileN;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          tc::mma_f16(d, kmajor_desc(q_addr, kk), kmajor_desc(kb, kk), kIdescS, kk > 0);
+        tc::commit(&s_full[j & 1]);
+        tc::commit(&kv_empty[st]);
+        return true;
+      };
+      ok = mbar_wait(q_full, 0);
+      if (ok) {
+        tc::fence_after_sync();
+        ok = issue_s(0);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1))) break;
+        const int u = 2 * j + 1;
+        const int st = u % kStages;
+        if (!(ok = mbar_wait(&kv_full[st], (u / kStages) & 1))) break;
+        tc::fence_after_sync();
+        const uint32_t pb = p_addr + (uint32_t)(j & 1) * kTileBytes;
+        const uint32_t vb = kv_addr + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          tc::mma_f16(tmem + kColO, kmajor_desc(pb, kk), vmn_desc(vb, kk), kIdescO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&o_done[j & 1]);
+        tc::commit(&kv_empty[st]);
+      }
+      // Every MMA issued above completes before tensor memory is released.
+      tc::commit(drain);
+      mbar_wait(drain, 0);
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    const int pos = pos0 + row;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int sb = j & 1;
+      if (!(ok = __all_sync(kFull, mbar_wait(&s_full[sb], (j >> 1) & 1)))) break;
+      tc::fence_after_sync();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::ld_32x32(tmem + t_lane + sb * kTileN + c * 32, sr[c]);
+      tc::wait_ld();
+      const int kbase = j * kTileN;
+      const bool need_mask = kbase + kTileN - 1 > pos0;  // diagonal tile(s)
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = __uint_as_float(sr[c][i]) * sl2;
+          if (need_mask && kbase + c * 32 + i > pos) v = -INFINITY;
+          sr[c][i] = __float_as_uint(v);
+          mt = fmaxf(mt, v);
+        }
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool resc = m_new > m + 8.0f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = fast_exp2(m - m_new);
+        m = m_new;
+        l *= alpha;
+      }
+      if (j > 0 && __any_sync(kFull, resc)) {
+        // The previous P V must have landed before the output row is rescaled.
+        if (!(ok = __all_sync(kFull, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))))
+          break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32(tmem + t_lane + kColO + c * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tc::st_32x32(tmem + t_lane + kColO + c * 32, o);
+        }
+        tc::wait_st();
+      }
+      // P buffer sb is free once P_{j-2} V_{j-2} has completed.
+      if (j >= 2 && !(ok = __all_sync(kFull, mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1))))
+        break;
+      uint8_t* prow = sP + sb * kTileBytes + row * 128;
+      float rs = 0.f;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunks of 8 keys
+        uint32_t pk4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k0 = c16 * 8 + 2 * e;
+          const float p0 = fast_exp2(__uint_as_float(sr[k0 >> 5][k0 & 31]) - m);
+          const float p1 = fast_exp2(__uint_as_float(sr[(k0 + 1) >> 5][(k0 + 1) & 31]) - m);
+          rs += p0 + p1;
+          __half2 hp = __floats2half2_rn(p0, p1);
+          pk4[e] = *reinterpret_cast<uint32_t*>(&hp);
+        }
+        const int slab = c16 >> 3, cc = c16 & 7;
+        *reinterpret_cast<uint4*>(prow + slab * kSlabBytes + ((cc ^ (row & 7)) << 4)) =
+            make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
+      }
+      l += rs;
+      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[sb]);
+    }
+    if (ok)
+      ok = __all_sync(kFull, mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = 1.f / l;
+      __half* orow = a.out + (out_row0 + row) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tc::ld_32x32(tmem + t_lane + kColO + c * 32, o);
+        tc::wait_ld();
+        uint32_t hv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __half2 t = __floats2half2_rn(__uint_as_float(o[2 * i]) * inv,
+                                        __uint_as_float(o[2 * i + 1]) * inv);
+          hv[i] = *reinterpret_cast<uint32_t*>(&t);
+        }
+        if (row < rows) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  // All roles meet here.  After a bounded wait gave up anywhere, the producer
+  // lets the copies it still has in flight land (again bounded) before the
+  // CTA's shared memory is released.
+  tc::fence_before_sync();
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) flag_status(a.status, PA_DEV_TIMEOUT);
+    if (warp == 0 && lane == 0) {
+      mbar_wait(q_full, 0);
+      for (int u = max(0, issued - kStages); u < issued; ++u)
+        mbar_wait(&kv_full[u % kStages], (u / kStages) & 1);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BS>
+cudaError_t launch_prefill_t(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                             cudaStream_t stream) {
+  CUtensorMap qmap, kmap, vmap;
+  const long long rows = (long long)a.num_blocks * BS;
+  cudaError_t e;
+  {
+    unsigned long long dims[3] = {(unsigned long long)kD, (unsigned long long)a.Lq,
+                                  (unsigned long long)a.B * a.H};
+    unsigned long long strides[2] = {(unsigned long long)kD * 2,
+                                     (unsigned long long)a.Lq * kD * 2};
+    unsigned box[3] = {64, kTileM, 1};
+    e = make_map_3d(&qmap, a.q, dims, strides, box, true);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    unsigned long long dims[3] = {(unsigned long long)kD, (unsigned long long)a.H,
+                                  (unsigned long long)rows};
+    unsigned long long strides[2] = {(unsigned long long)kD * 2,
+                                     (unsigned long long)a.H * kD * 2};
+    unsigned box[3] = {64, 1, (unsigned)BS};
+    e = make_map_3d(&kmap, k_cache, dims, strides, box, true);
+    if (e != cudaSuccess) return e;
+    e = make_map_3d(&vmap, v_cache, dims, strides, box, true);
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = prefill_kernel<BS>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.Lq + kTileM - 1) / kTileM, a.H, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
+}
+
+}  // namespace
+
+bool prefill_supported(int D, int block_size) {
+  return D == kD && (block_size == 16 || block_size == 32);
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                           cudaStream_t stream) {
+  if (a.H > 65535 || a.B > 65535) return cudaErrorInvalidValue;
+  if (a.block_size == 16) return launch_prefill_t<16>(a, k_cache, v_cache, stream);
+  if (a.block_size == 32) return launch_prefill_t<32>(a, k_cache, v_cache, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pk

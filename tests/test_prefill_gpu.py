@@ -1,0 +1,140 @@
+"""Parity of pa_prefill_chunk (tcgen05 tensor-core kernel) with the fp64 oracle.
+
+The chunk's Lq queries are the last Lq positions of each sequence; query i
+sees keys 0 .. ctx-Lq+i.  Cases go from one 128x128 tile up to the
+8-sequence, 512-query chunk on a 3,584-token paged context.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_172_gb300 as pk
+from paged_kv_cache_172_gb300 import workloads
+from pk_testutil import assert_close, errors, to_dev, zero_status
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(DEV)
+
+
+def run_prefill(g, scale, status=None, out=None):
+    return pk.pa_prefill_chunk(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                               g["context_lens"], scale, status=status, out=out)
+
+
+def check_against_oracle(B, H, bs, Lq, ctx, seed, what):
+    batch = workloads.random_prefill(B, H, 128, bs, Lq, ctx, seed=seed, device="cpu",
+                                     write_chunk=False)
+    ref = oracle.prefill(batch.q.numpy(), batch.k_cache.numpy(), batch.v_cache.numpy(),
+                         batch.block_tables.numpy(), batch.context_lens.numpy(), batch.scale)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out = run_prefill(g, batch.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return assert_close(out, ref, what=what)
+
+
+def test_prefill_one_tile():
+    check_against_oracle(1, 1, 16, 128, [128], seed=40, what="one 128x128 tile")
+
+
+def test_prefill_two_key_tiles():
+    check_against_oracle(1, 2, 16, 128, [256], seed=41, what="two key tiles")
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("Lq,ctx", [(1, [1, 77]), (100, [100, 300]), (200, [333, 200]),
+                                    (256, [1000, 700]), (37, [4096, 37])])
+def test_prefill_ragged(bs, Lq, ctx):
+    check_against_oracle(len(ctx), 3, bs, Lq, ctx, seed=42 + Lq, what=f"bs={bs} Lq={Lq} {ctx}")
+
+
+def test_prefill_lq1_matches_decode():
+    batch = workloads.random_prefill(4, 8, 128, 16, 1, [1, 129, 2000, 640], seed=50,
+                                     device=DEV, write_chunk=False)
+    g = to_dev(batch, DEV)
+    a = run_prefill(g, batch.scale)[:, :, 0]
+    b = pk.pa_decode(g["q"][:, :, 0].contiguous(), g["k_cache"], g["v_cache"],
+                     g["block_tables"], g["context_lens"], batch.scale, 2000)
+    assert (a.float() - b.float()).abs().max().item() <= 2e-3
+
+
+def test_prefill_permutation_invariance_bit_exact():
+    batch = workloads.random_prefill(2, 4, 128, 16, 160, [600, 300], seed=51, device="cpu",
+                                     write_chunk=False)
+    g = to_dev(batch, DEV)
+    out = run_prefill(g, batch.scale)
+    perm = torch.randperm(batch.num_blocks, generator=torch.Generator().manual_seed(5))
+    k2 = torch.empty_like(batch.k_cache)
+    v2 = torch.empty_like(batch.v_cache)
+    k2[perm] = batch.k_cache
+    v2[perm] = batch.v_cache
+    bt = batch.block_tables.long()
+    t2 = torch.where(bt >= 0, perm[bt.clamp(min=0)], torch.full_like(bt, -1)).int()
+    out2 = run_prefill(dict(g, k_cache=k2.to(DEV), v_cache=v2.to(DEV),
+                            block_tables=t2.to(DEV)), batch.scale)
+    assert torch.equal(out, out2)
+
+
+def test_prefill_value_ones_and_bad_context():
+    batch = workloads.random_prefill(2, 2, 128, 16, 130, [500, 130], seed=52, device=DEV,
+                                     write_chunk=False)
+    g = to_dev(batch, DEV)
+    out = run_prefill(dict(g, v_cache=torch.ones_like(g["v_cache"])), batch.scale)
+    assert torch.all(out == 1.0)
+    status = zero_status(DEV)
+    bad = g["context_lens"].clone()
+    bad[1] = 129  # shorter than the chunk
+    out = torch.full_like(g["q"], 3.0)
+    run_prefill(dict(g, context_lens=bad), batch.scale, status=status, out=out)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pk.PA_DEV_BAD_CONTEXT
+    assert torch.all(out[1] == 0)
+
+
+def test_chunked_prefill_workload():
+    """8 x 512 queries on 3,584 cached tokens, 40 heads: chunk K/V written by
+    pa_kv_cache_write first; oracle on whole (b, h) rows of two heads and on
+    sampled rows (tile and mask edges) of every (b, h)."""
+    batch = workloads.chunked_prefill(seed=4, device=DEV)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    kc0 = batch.k_cache.cpu().numpy()
+    vc0 = batch.v_cache.cpu().numpy()
+    pk.pa_kv_cache_write(g["k_new"], g["v_new"], g["slot_mapping"], g["k_cache"], g["v_cache"],
+                         status=status)
+    out = run_prefill(g, batch.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    kc, vc = oracle.kv_cache_write(batch.k_new.cpu().numpy(), batch.v_new.cpu().numpy(),
+                                   batch.slot_mapping.cpu().numpy(), kc0, vc0)
+    assert np.array_equal(g["k_cache"].cpu().numpy().view(np.uint16), kc)
+    q = batch.q.cpu().numpy()
+    tables = batch.block_tables.cpu().numpy()
+    ctx = batch.context_lens.cpu().numpy()
+    Lq = q.shape[2]
+    got = out.float().cpu().numpy()
+    errs = []
+    for (b, h) in [(0, 0), (5, 33)]:  # whole rows
+        for i in range(Lq):
+            ref = oracle.attend_row(q[b, h, i], kc, vc, tables[b], ctx[b] - Lq + i + 1, h,
+                                    batch.scale)
+            errs.append(np.abs(got[b, h, i] - ref))
+    rows = [0, 1, 126, 127, 128, 129, 255, 256, 383, 384, 510, 511]
+    for b in range(q.shape[0]):
+        for h in range(0, q.shape[1], 3):
+            for i in rows:
+                ref = oracle.attend_row(q[b, h, i], kc, vc, tables[b], ctx[b] - Lq + i + 1, h,
+                                        batch.scale)
+                errs.append(np.abs(got[b, h, i] - ref))
+    err = np.concatenate(errs)
+    print(f"chunked prefill: {len(errs)} rows, max|err| {err.max():.2e} mean {err.mean():.2e}")
+    assert err.max() <= 5e-3 and err.mean() <= 5e-4
