@@ -345,6 +345,162 @@ def workload_config(batch, pt, l2):
             "sum_context_len": int(ctx.sum()), "partition_tokens": pt, "l2": l2}
 
 
+# ---------------------------------------------------------------------------
+# auxiliary workloads (measurement lines for the other paged-attention cases;
+# the default line above stays the 38-sequence decode)
+# ---------------------------------------------------------------------------
+def prefill_flops(ctx, Lq, H, D):
+    """Useful causal FLOPs: query i of the chunk sees ctx-Lq+i+1 keys; each
+    (query, key) pair costs 2*D for Q K^T and 2*D for P V."""
+    total = 0
+    for n in ctx:
+        n = int(n)
+        total += Lq * (n - Lq + 1) + Lq * (Lq - 1) // 2
+    return 4 * D * H * total
+
+
+def unique_kv_bytes(tables, ctx, bs, H, D):
+    """K+V bytes of the distinct physical rows the batch attends to."""
+    used = {}
+    for b, n in enumerate(ctx):
+        n = int(n)
+        for lb in range(-(-n // bs)):
+            phys = int(tables[b, lb])
+            used[phys] = max(used.get(phys, 0), min(bs, n - lb * bs))
+    return sum(used.values()) * H * D * 2 * 2
+
+
+def run_aux(args, name):
+    import paged_kv_cache_172_gb300 as pk
+    from paged_kv_cache_172_gb300 import build_lib, workloads
+
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+    peak_hbm, hbm_kind = measured_peak()
+    if name == "prefix_sharing":
+        batch = workloads.prefix_sharing(seed=2, device=dev)
+        lay = batch.meta["layout"]
+        ctx = lay.context_lens
+        max_ctx = int(ctx.max())
+        out = torch.empty_like(batch.q)
+        H, D, bs = batch.H, batch.D, batch.block_size
+        phases = [
+            ("block_copy", lambda: pk.pa_block_copy(batch.k_cache, batch.v_cache,
+                                                    batch.copy_pairs, status=status,
+                                                    stream=stream)),
+            ("decode", lambda: pk.pa_decode(batch.q, batch.k_cache, batch.v_cache,
+                                            batch.block_tables, batch.context_lens,
+                                            batch.scale, max_ctx, out=out, status=status,
+                                            stream=stream)),
+        ]
+        logical = decode_bytes(ctx, batch.B, H, D, bs)
+        unique = unique_kv_bytes(lay.tables, ctx, bs, H, D) + 2 * batch.B * H * D * 2
+        copy_bytes = 2 * 2 * len(lay.pairs) * bs * H * D * 2
+        main, work, unit, bound = "decode", unique, "GB/s", "hbm"
+        extra = {"logical_bytes": logical, "unique_bytes": unique, "copy_bytes": copy_bytes}
+        desc = ("prefix_sharing_16x8: 16 prompts x 8 samples, 1024-token shared prompts, "
+                "tails U[1,512], 40 heads, head_dim 128, block_size 16; step = block_copy of "
+                "128 copy-on-write blocks + pa_decode; GB/s on unique bytes")
+    elif name == "long_context":
+        batch = workloads.long_context(seed=3, device=dev)
+        n = int(batch.context_lens[0])
+        out = torch.empty_like(batch.q)
+        H, D, bs = batch.H, batch.D, batch.block_size
+        phases = [("decode", lambda: pk.pa_decode(batch.q, batch.k_cache, batch.v_cache,
+                                                  batch.block_tables, batch.context_lens,
+                                                  batch.scale, n, out=out, status=status,
+                                                  stream=stream))]
+        work = decode_bytes([n], 1, H, D, bs)
+        main, unit, bound, extra = "decode", "GB/s", "hbm", {}
+        desc = ("long_context_1M: 1 sequence of 1,048,576 tokens, 40 heads, head_dim 128, "
+                "block_size 16, 65,536 permuted blocks; split-KV decode")
+    elif name == "chunked_prefill":
+        batch = workloads.chunked_prefill(seed=4, device=dev)
+        ctx = batch.context_lens.cpu().numpy()
+        out = torch.empty_like(batch.q)
+        B, H, Lq, D = batch.q.shape
+        bs = batch.block_size
+        phases = [
+            ("kv_cache_write", lambda: pk.pa_kv_cache_write(batch.k_new, batch.v_new,
+                                                            batch.slot_mapping, batch.k_cache,
+                                                            batch.v_cache, status=status,
+                                                            stream=stream)),
+            ("prefill", lambda: pk.pa_prefill_chunk(batch.q, batch.k_cache, batch.v_cache,
+                                                    batch.block_tables, batch.context_lens,
+                                                    batch.scale, out=out, status=status,
+                                                    stream=stream)),
+        ]
+        work = prefill_flops(ctx, Lq, H, D)
+        main, unit, bound = "prefill", "TFLOP/s", "tensor"
+        extra = {"useful_flops": work,
+                 "kv_bytes": int(ctx.sum()) * H * D * 4, "q_out_bytes": 2 * batch.q.numel() * 2}
+        desc = ("chunked_prefill_8x512_on_3584: 8 sequences, 512-query chunk on 3,584 cached "
+                "tokens (context 4,096), 40 heads, head_dim 128, block_size 16; step = "
+                "kv_cache_write of the 4,096 chunk tokens + pa_prefill_chunk")
+    else:
+        raise SystemExit(f"unknown workload {name}")
+
+    def run_step(evs=None):
+        for i, (_, fn) in enumerate(phases):
+            if evs is not None:
+                evs[i].record(stream)
+            fn()
+        if evs is not None:
+            evs[-1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            torch.sum(flush, dim=0, out=flush_sink)
+            run_step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+           for _ in range(K)]
+    with ClockSampler(0) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                torch.sum(flush, dim=0, out=flush_sink)
+                run_step(evs[i])
+        torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+    phase_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, (nm, _) in enumerate(phases)}
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
+    main_s = phase_ms[main] / 1e3
+    if bound == "tensor":
+        achieved = work / main_s / 1e12
+        peak, peak_kind = 1904.1, "measured bf16 burst (fp16 dense rate equal)"
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                peak = float(json.load(f)["bf16_tflops"])
+        except Exception:
+            peak, peak_kind = 1900.0, "fallback"
+    else:
+        achieved = work / main_s / 1e9
+        peak, peak_kind = peak_hbm, hbm_kind
+    line = {
+        "metric": f"{name} {unit}", "value": achieved, "unit": unit, "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "dtype": "f16 storage, f32 accumulate", "data": "synthetic (seeded fp16 N(0,1))",
+        "config": {"workload": desc, "l2": "flushed before every timed step (512 MB read)"},
+        "phase_ms": phase_ms,
+        "roofline": {"bound": bound, "kernel": main, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": None},
+        "clocks": clocks.summary(),
+    }
+    line.update(extra)
+    if name == "prefix_sharing":
+        line["logical_GBs"] = logical / main_s / 1e9
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -355,6 +511,9 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="llama13b_decode",
+                    choices=["llama13b_decode", "prefix_sharing", "long_context",
+                             "chunked_prefill"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -365,6 +524,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.workload != "llama13b_decode":
+        run_aux(args, args.workload)
         return
 
     if world > 1:

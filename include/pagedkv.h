@@ -171,7 +171,7 @@ pa_status pa_decode_static(const pa_half *q, const pa_half *k_cache,
  *
  * q   [B, H, Lq, D] fp16 (the blog's [batch, heads, seq_len, head_dim])
  * out [B, H, Lq, D] fp16
- * context_lens[b] in [Lq, max_blocks_per_seq * block_size].
+ * context_lens[b] in [Lq, max_blocks_per_seq * block_size]; scale > 0.
  * D == 128 and block_size in {16, 32} run on the tcgen05 tensor-core kernel;
  * other supported (D, block_size) pairs return PA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */

@@ -197,7 +197,8 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
                            const int32_t* block_tables, const int32_t* context_lens, int B, int H,
                            int Lq, int D, int block_size, int num_blocks, int max_blocks_per_seq,
                            float scale, pa_half* out, int32_t* status, pa_stream_t stream) {
-  if (B < 0 || H <= 0 || Lq < 0 || max_blocks_per_seq <= 0 || !isfinite(scale))
+  if (B < 0 || H <= 0 || Lq < 0 || max_blocks_per_seq <= 0 || !isfinite(scale) ||
+      !(scale > 0.f))
     return PA_ERR_INVALID;
   if (!pk::prefill_supported(D, block_size)) return PA_ERR_UNSUPPORTED;
   if (B == 0 || Lq == 0) return PA_OK;

@@ -125,6 +125,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ---- misc --------------------------------------------------------------------
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// 2^x with the hardware approximation (flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int N>
 struct Log2 {
   static constexpr int value = 1 + Log2<N / 2>::value;

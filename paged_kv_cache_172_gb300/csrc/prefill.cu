@@ -7,26 +7,30 @@
 // Lq chunk queries sit at positions n-Lq .. n-1 and query i sees keys
 // 0 .. n-Lq+i).
 //
-// One CTA = 128 queries of one (sequence, head); it walks the visible keys in
-// tiles of 128 (8 blocks of 16 or 4 of 32 tokens):
-//   warp 0      TMA producer: Q once (2 x 64-dim slabs, 128-byte swizzle),
-//               then per key tile one box per (block, 64-dim slab) for K and
-//               for V, gathered through the block table, into a 4-stage ring;
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a double-buffered
-//               TMEM tile (8 x K=16 tcgen05.mma), then O += P_j V_j into the
-//               TMEM output accumulator once the softmax has written P_j;
-//               S_{j+1} is issued before waiting for P_j so the tensor core
-//               works on the next tile while the softmax runs;
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): load the
-//               row of S_j from TMEM, scale into the log2 domain, mask the
-//               diagonal tile, update the running max, write P_j (fp16) to a
-//               swizzled shared-memory tile for the next MMA.  The output
-//               accumulator is rescaled only when the max grows by more than
-//               2^8 (P then stays <= 256, exact in fp16 range), so most tiles
-//               skip the TMEM read-modify-write.  Epilogue: O / l -> fp16.
+// One CTA = 256 queries (two 128-row tiles A and B) of one (sequence, head);
+// it walks the visible keys in tiles of 128 (8 blocks of 16 or 4 of 32):
+//   warps 0-3   softmax of tile A, one query row per thread (TMEM lane = row);
+//   warps 4-7   softmax of tile B;
+//   warp 8      TMA producer: Q (4 boxes of 128 rows x 64 dims, 128-byte
+//               swizzle), then per key tile one box per (block, 64-dim half)
+//               for K and for V, gathered through the block table, into a
+//               3-stage ring shared by both Q tiles;
+//   warp 9      MMA issuer (one thread) and tensor-memory owner, in ping-pong
+//               order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while one tile's
+//               softmax runs the tensor core works on the other tile.
+// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Because tcgen05 operations of one thread complete in issue order, "S_X(j+1)
+// done" implies "P_X(j) V_j done": the softmax may then rescale O_X and
+// overwrite P_X without any further barrier.
+// Softmax per tile: pass 1 loads the S row from TMEM and takes the row max
+// (keys past the row's position masked on diagonal tiles); the output
+// accumulator is rescaled only when the max grows by more than 2^8 (P then
+// stays <= 256, exact in fp16 range); pass 2 reloads S, forms
+// p = 2^(s*scale*log2e - m) with one FMA and one ex2 per element, sums the
+// row and writes P (fp16) into a swizzled shared-memory tile.
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle):
-//   Q, K_j, P_j : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
-//                 the two 64-dim (or 64-key) halves 16 KB apart;
+//   Q, K_j, P   : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
+//                 the two 64-element halves 16 KB apart;
 //   V_j         : MN-major (dims contiguous): 8-key atoms 1024 B apart along
 //                 K, the two 64-dim halves 16 KB apart along N.
 #include "pk_common.cuh"
@@ -38,20 +42,22 @@ namespace pk {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kTileM = 128;                  // queries per CTA
+constexpr int kTileM = 128;                  // queries per Q tile (two per CTA)
 constexpr int kTileN = 128;                  // keys per tile
 constexpr int kD = 128;                      // head dim
 constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
 constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
-constexpr int kStages = 4;                   // K/V ring (K and V tiles alternate)
-constexpr int kThreads = 192;
+constexpr int kStages = 3;                   // K/V ring (K and V tiles alternate)
+constexpr int kThreads = 320;                // 8 softmax warps + producer + MMA
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 constexpr int kTblWindow = 256;              // block-table entries staged in smem
-constexpr int kTmemCols = 512;               // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTileBytes;
-constexpr int kOffP = kOffKV + kStages * kTileBytes;
+constexpr int kOffQ = 0;                                // Q_A, Q_B
+constexpr int kOffKV = kOffQ + 2 * kTileBytes;
+constexpr int kOffP = kOffKV + kStages * kTileBytes;   // P_A, P_B
 constexpr int kOffBar = kOffP + 2 * kTileBytes;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
 constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
@@ -89,31 +95,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
+  uint64_t* s_full = kv_empty + kStages;  // [2]: per Q tile
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* o_done = p_full + 2;          // [2]
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
   int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int ct = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
 
   pdl_wait();  // inputs may come from the previous kernel on the stream
   const int n = a.context_lens[b];
-  const int q0 = qt * kTileM;
-  const int rows = min(kTileM, a.Lq - q0);
+  const int q0 = ct * 2 * kTileM;
+  const int rows_all = min(2 * kTileM, a.Lq - q0);
   const size_t out_row0 = ((size_t)b * a.H + h) * a.Lq + q0;
   if (n < a.Lq || n > a.max_blocks * BS) {
     if (threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
     uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * kD);
-    for (int i = threadIdx.x; i < rows * (kD / 8); i += kThreads) o4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < rows_all * (kD / 8); i += kThreads)
+      o4[i] = make_uint4(0, 0, 0, 0);
     return;
   }
-  const int pos0 = n - a.Lq + q0;        // sequence position of query row 0
-  const int last_key = pos0 + rows - 1;  // last key any valid row sees
-  const int n_tiles = last_key / kTileN + 1;
+  // Per Q tile (A = 0, B = 1): rows, sequence position of row 0, key tiles.
+  const int rows_a = min(kTileM, a.Lq - q0);
+  const int rows_b = max(0, min(kTileM, a.Lq - (q0 + kTileM)));
+  const int pos0_a = n - a.Lq + q0;
+  const int pos0_b = pos0_a + kTileM;
+  const int ntile_a = (pos0_a + rows_a - 1) / kTileN + 1;
+  const int ntile_b = rows_b > 0 ? (pos0_b + rows_b - 1) / kTileN + 1 : 0;
+  const int n_kv = max(ntile_a, ntile_b);
   const int nblk_seq = (n + BS - 1) / BS;
 
   if (threadIdx.x == 0) {
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc::tmem_alloc(tmem_holder, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -141,16 +153,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   int issued = 0;  // K/V tiles the producer issued into the ring
 
-  if (warp == 0) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     int win = -kTblWindow;
     if (lane == 0) {
       const int bh = b * a.H + h;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_3d(sQ, &qmap, 0, q0, bh, q_full);
-      tma_load_3d(sQ + kSlabBytes, &qmap, 64, q0, bh, q_full);
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        tma_load_3d(sQ + x * kTileBytes, &qmap, 0, q0 + x * kTileM, bh, q_full);
+        tma_load_3d(sQ + x * kTileBytes + kSlabBytes, &qmap, 64, q0 + x * kTileM, bh, q_full);
+      }
     }
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    for (int j = 0; j < n_kv && ok; ++j) {
       const int lb0 = j * BPT;
       if (lb0 + BPT > win + kTblWindow) {
         win = lb0;
@@ -190,141 +205,164 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(kFull, ok, 0);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
-      auto issue_s = [&](int j) -> bool {
+      // S_X(j) = Q_X K_j^T; releases K_j when X is its last user.
+      auto issue_s = [&](int x, int j, bool release) -> bool {
         const int u = 2 * j;
         const int st = u % kStages;
         if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
         tc::fence_after_sync();
+        const uint32_t qa = q_addr + x * kTileBytes;
         const uint32_t kb = kv_addr + st * kTileBytes;
-        const uint32_t d = tmem + (uint32_t)(j & 1) * kTileN;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          tc::mma_f16(d, kmajor_desc(q_addr, kk), kmajor_desc(kb, kk), kIdescS, kk > 0);
-        tc::commit(&s_full[j & 1]);
-        tc::commit(&kv_empty[st]);
+          tc::mma_f16(tmem + x * kTileN, kmajor_desc(qa, kk), kmajor_desc(kb, kk), kIdescS,
+                      kk > 0);
+        tc::commit(&s_full[x]);
+        if (release) tc::commit(&kv_empty[st]);
+        return true;
+      };
+      // O_X += P_X V_j once the softmax of X has written P_X for tile j.
+      auto issue_pv = [&](int x, int j, int ntile) -> bool {
+        if (!mbar_wait(&p_full[x], j & 1)) return false;
+        const int u = 2 * j + 1;
+        const int st = u % kStages;
+        if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t pb = p_addr + x * kTileBytes;
+        const uint32_t vb = kv_addr + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          tc::mma_f16(tmem + kColO + x * kD, kmajor_desc(pb, kk), vmn_desc(vb, kk), kIdescO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        if (j == ntile - 1) tc::commit(&o_done[x]);
         return true;
       };
       ok = mbar_wait(q_full, 0);
       if (ok) {
         tc::fence_after_sync();
-        ok = issue_s(0);
+        ok = issue_s(0, 0, ntile_b == 0);
+        if (ok && ntile_b > 0) ok = issue_s(1, 0, true);
       }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1))) break;
-        const int u = 2 * j + 1;
-        const int st = u % kStages;
-        if (!(ok = mbar_wait(&kv_full[st], (u / kStages) & 1))) break;
-        tc::fence_after_sync();
-        const uint32_t pb = p_addr + (uint32_t)(j & 1) * kTileBytes;
-        const uint32_t vb = kv_addr + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          tc::mma_f16(tmem + kColO, kmajor_desc(pb, kk), vmn_desc(vb, kk), kIdescO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&o_done[j & 1]);
-        tc::commit(&kv_empty[st]);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j < ntile_a && !(ok = issue_pv(0, j, ntile_a))) break;
+        if (j + 1 < ntile_a && !(ok = issue_s(0, j + 1, j + 1 >= ntile_b))) break;
+        if (j < ntile_b && !(ok = issue_pv(1, j, ntile_b))) break;
+        tc::commit(&kv_empty[(2 * j + 1) % kStages]);  // V_j has no further reader
+        if (j + 1 < ntile_b && !(ok = issue_s(1, j + 1, true))) break;
       }
-      // Every MMA issued above completes before tensor memory is released.
-      tc::commit(drain);
-      mbar_wait(drain, 0);
     }
     ok = __shfl_sync(kFull, ok, 0);
   } else {
     // ------------------------------------------------------------ softmax
+    const int x = warp >> 2;       // Q tile of this warpgroup
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_s = tmem + t_lane + x * kTileN;
+    const uint32_t t_o = tmem + t_lane + kColO + x * kD;
+    const int pos0 = x ? pos0_b : pos0_a;
     const int pos = pos0 + row;
+    const int ntile = x ? ntile_b : ntile_a;
+    const int rows = x ? rows_b : rows_a;
     const float sl2 = a.scale_log2;
+    uint8_t* prow = sP + x * kTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int sb = j & 1;
-      if (!(ok = __all_sync(kFull, mbar_wait(&s_full[sb], (j >> 1) & 1)))) break;
+    for (int j = 0; j < ntile && ok; ++j) {
+      if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::ld_32x32(tmem + t_lane + sb * kTileN + c * 32, sr[c]);
-      tc::wait_ld();
       const int kbase = j * kTileN;
-      const bool need_mask = kbase + kTileN - 1 > pos0;  // diagonal tile(s)
-      float mt = -INFINITY;
+      const bool diag = kbase + kTileN - 1 > pos0;  // some key here is past some row
+      // pass 1: row max of the raw scores (scale > 0 keeps the order)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld_32x32(t_s + c * 32, r);
+        tc::wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(sr[c][i]) * sl2;
-          if (need_mask && kbase + c * 32 + i > pos) v = -INFINITY;
-          sr[c][i] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i <= pos) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
         }
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + 8.0f;
       float alpha = 1.f;
       if (resc) {
-        alpha = fast_exp2(m - m_new);
+        alpha = ex2_approx(m - m_new);
         m = m_new;
         l *= alpha;
       }
       if (j > 0 && __any_sync(kFull, resc)) {
-        // The previous P V must have landed before the output row is rescaled.
-        if (!(ok = __all_sync(kFull, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))))
-          break;
-        tc::fence_after_sync();
+        // S_X(j) has completed, hence so has P_X(j-1) V_{j-1}: rescale O_X.
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tc::ld_32x32(tmem + t_lane + kColO + c * 32, o);
+          tc::ld_32x32(t_o + c * 32, o);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tc::st_32x32(tmem + t_lane + kColO + c * 32, o);
+          tc::st_32x32(t_o + c * 32, o);
         }
         tc::wait_st();
       }
-      // P buffer sb is free once P_{j-2} V_{j-2} has completed.
-      if (j >= 2 && !(ok = __all_sync(kFull, mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1))))
-        break;
-      uint8_t* prow = sP + sb * kTileBytes + row * 128;
-      float rs = 0.f;
+      // pass 2: P = 2^(s * scale * log2e - m) in fp16, row sum
+      const float neg_m = -m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {  // 16-byte chunks of 8 keys
-        uint32_t pk4[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld_32x32(t_s + c * 32, r);
+        tc::wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k0 = c16 * 8 + 2 * e;
-          const float p0 = fast_exp2(__uint_as_float(sr[k0 >> 5][k0 & 31]) - m);
-          const float p1 = fast_exp2(__uint_as_float(sr[(k0 + 1) >> 5][(k0 + 1) & 31]) - m);
-          rs += p0 + p1;
-          __half2 hp = __floats2half2_rn(p0, p1);
-          pk4[e] = *reinterpret_cast<uint32_t*>(&hp);
+        for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte chunks of 8 keys
+          uint32_t pk4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = q8 * 8 + 2 * e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(r[i0]), sl2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(r[i0 + 1]), sl2, neg_m));
+            if (diag) {
+              if (kbase + c * 32 + i0 > pos) p0 = 0.f;
+              if (kbase + c * 32 + i0 + 1 > pos) p1 = 0.f;
+            }
+            rs[e] += p0 + p1;
+            __half2 hp = __floats2half2_rn(p0, p1);
+            pk4[e] = *reinterpret_cast<uint32_t*>(&hp);
+          }
+          const int c16 = c * 4 + q8;  // chunk index 0..15 along the keys
+          const int slab = c16 >> 3, cc = c16 & 7;
+          *reinterpret_cast<uint4*>(prow + slab * kSlabBytes + ((cc ^ (row & 7)) << 4)) =
+              make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
         }
-        const int slab = c16 >> 3, cc = c16 & 7;
-        *reinterpret_cast<uint4*>(prow + slab * kSlabBytes + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
       }
-      l += rs;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
       tc::fence_before_sync();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[x]);
     }
-    if (ok)
-      ok = __all_sync(kFull, mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1));
-    if (ok) {
+    if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&o_done[x], 0));
+    if (ok && ntile > 0) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
-      __half* orow = a.out + (out_row0 + row) * kD;
+      __half* orow = a.out + (out_row0 + x * kTileM + row) * kD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tc::ld_32x32(tmem + t_lane + kColO + c * 32, o);
+        tc::ld_32x32(t_o + c * 32, o);
         tc::wait_ld();
         uint32_t hv[16];
 #pragma unroll
@@ -344,19 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // All roles meet here.  After a bounded wait gave up anywhere, the producer
-  // lets the copies it still has in flight land (again bounded) before the
-  // CTA's shared memory is released.
+  // lets the copies it still has in flight land and the MMA issuer waits for
+  // its last MMAs (both bounded) before shared and tensor memory are released.
   tc::fence_before_sync();
   if (__syncthreads_or(!ok)) {
     if (threadIdx.x == 0) flag_status(a.status, PA_DEV_TIMEOUT);
-    if (warp == 0 && lane == 0) {
+    if (warp == kWarpProducer && lane == 0) {
       mbar_wait(q_full, 0);
       for (int u = max(0, issued - kStages); u < issued; ++u)
         mbar_wait(&kv_full[u % kStages], (u / kStages) & 1);
     }
+    if (warp == kWarpMma && lane == 0) {
+      tc::commit(drain);
+      mbar_wait(drain, 0);
+    }
     __syncthreads();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -396,7 +438,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const void* k_cache, const vo
     attr_done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Lq + kTileM - 1) / kTileM, a.H, a.B);
+  cfg.gridDim = dim3((a.Lq + 2 * kTileM - 1) / (2 * kTileM), a.H, a.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;

@@ -108,6 +108,10 @@ def test_prefill_validation(lib):
     rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, -2, 4, 8, 128, 16, 8, 4,
                               0.1, 0x1000, NULL, NULL)
     assert rc == pk.PA_ERR_INVALID
+    for bad_scale in (0.0, -0.5, float("inf")):  # the prefill kernel needs scale > 0
+        rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 128, 16, 8,
+                                  4, bad_scale, 0x1000, NULL, NULL)
+        assert rc == pk.PA_ERR_INVALID
 
 
 def test_binding_rejects_cpu_tensors():
