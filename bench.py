@@ -37,10 +37,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 
-# dram__bytes_read.sum + dram__bytes_write.sum per pa_decode call (partition +
-# combine kernels) from one ncu capture of the 38-sequence batch, keyed by the
-# hash of the decode source it was taken on; null once the source changes.
-DECODE_TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the decode
+# partition kernel (the dominant kernel) from an ncu capture of this bench's
+# 38-sequence batch, keyed by the hash of the decode source it was taken on;
+# null once the source changes.
+DECODE_TRAFFIC = {"550f896f0f934f59": 852442624 + 5792512}
 
 
 def src_hash(name):
@@ -501,6 +502,20 @@ def run_aux(args, name):
     print(json.dumps(line))
 
 
+def aggregate_ranks(timed_s, e2e_s, step_bytes, world, device):
+    """Whole-job numbers of N independent replicas: the slowest rank's times
+    (max over ranks) and the bytes of all ranks (sum).  Host-side only; the
+    data path has no collective."""
+    if world <= 1:
+        return timed_s, e2e_s, float(step_bytes)
+    t = torch.tensor([timed_s, e2e_s], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    b = torch.tensor([float(step_bytes)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(b)
+    timed_s, e2e_s = t.tolist()
+    return timed_s, e2e_s, b.item()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -536,16 +551,8 @@ def main():
     total_s = res["step_ms"] * K / 1e3
     step_bytes = res["step_bytes"]
     dec_s = res["decode_ms"] / 1e3
-    if world > 1:
-        t = torch.tensor([total_s, res["e2e_ms"] * K / 1e3], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s, e2e_s = t.tolist()
-        b = torch.tensor([float(step_bytes)], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(b)
-        all_bytes = b.item()
-    else:
-        e2e_s = res["e2e_ms"] * K / 1e3
-        all_bytes = float(step_bytes)
+    total_s, e2e_s, all_bytes = aggregate_ranks(total_s, res["e2e_ms"] * K / 1e3,
+                                                step_bytes, world, "cuda")
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
@@ -571,7 +578,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "pa_decode (partition + combine kernels)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes": res["decode_bytes"]},
+                     "traffic": traffic, "traffic_kernel": "partition_kernel",
+                     "algorithmic_bytes": res["decode_bytes"]},
         "e2e": {"value": all_bytes * K / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": e2e_s / K * 1e3},

@@ -14,22 +14,24 @@
 //   warp 8      TMA producer: Q (4 boxes of 128 rows x 64 dims, 128-byte
 //               swizzle), then per key tile one box per (block, 64-dim half)
 //               for K and for V, gathered through the block table, into a
-//               3-stage ring shared by both Q tiles;
+//               5-stage ring shared by both Q tiles (two key tiles ahead);
 //   warp 9      MMA issuer (one thread) and tensor-memory owner, in ping-pong
 //               order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while one tile's
 //               softmax runs the tensor core works on the other tile.
-// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
-// Because tcgen05 operations of one thread complete in issue order, "S_X(j+1)
-// done" implies "P_X(j) V_j done": the softmax may then rescale O_X and
-// overwrite P_X without any further barrier.
-// Softmax per tile: pass 1 loads the S row from TMEM and takes the row max
-// (keys past the row's position masked on diagonal tiles); the output
-// accumulator is rescaled only when the max grows by more than 2^8 (P then
-// stays <= 256, exact in fp16 range); pass 2 reloads S, forms
-// p = 2^(s*scale*log2e - m) with one FMA and one ex2 per element, sums the
-// row and writes P (fp16) into a swizzled shared-memory tile.
+// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512);
+// P_X (fp16 pairs packed per 32-bit column) overwrites the first 64 columns
+// of S_X once the softmax holds S_X in registers, and the P V MMA reads it
+// from tensor memory.  Because tcgen05 operations of one thread complete in
+// issue order, "S_X(j+1) done" implies "P_X(j) V_j done": the softmax may
+// then rescale O_X without any further barrier.
+// Softmax per tile: two tensor-memory round trips over the S row, one for
+// the row max (keys past the row's position skipped on diagonal tiles), one
+// for p = 2^(s*scale*log2e - m) (one FMA and one ex2 per element); between
+// them the output accumulator is rescaled, only when the row max grew by more
+// than 2^8 (P then stays <= 256, exact in fp16 range).  The row is summed and
+// P (fp16) stored to tensor memory.
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle):
-//   Q, K_j, P   : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
+//   Q, K_j      : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
 //                 the two 64-element halves 16 KB apart;
 //   V_j         : MN-major (dims contiguous): 8-key atoms 1024 B apart along
 //                 K, the two 64-dim halves 16 KB apart along N.
@@ -47,7 +49,7 @@ constexpr int kTileN = 128;                  // keys per tile
 constexpr int kD = 128;                      // head dim
 constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
 constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
-constexpr int kStages = 3;                   // K/V ring (K and V tiles alternate)
+constexpr int kStages = 5;                   // K/V ring (K and V tiles alternate)
 constexpr int kThreads = 320;                // 8 softmax warps + producer + MMA
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
@@ -57,8 +59,7 @@ constexpr uint32_t kColO = 256;
 
 constexpr int kOffQ = 0;                                // Q_A, Q_B
 constexpr int kOffKV = kOffQ + 2 * kTileBytes;
-constexpr int kOffP = kOffKV + kStages * kTileBytes;   // P_A, P_B
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kOffBar = kOffKV + kStages * kTileBytes;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
 constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
 constexpr int kOffTbl = (kOffTmemHolder + 4 + 15) / 16 * 16;
@@ -90,7 +91,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sKV = smem + kOffKV;
-  uint8_t* sP = smem + kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
@@ -210,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t kv_addr = smem_u32(sKV);
-      const uint32_t p_addr = smem_u32(sP);
       // S_X(j) = Q_X K_j^T; releases K_j when X is its last user.
       auto issue_s = [&](int x, int j, bool release) -> bool {
         const int u = 2 * j;
@@ -234,12 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = u % kStages;
         if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
         tc::fence_after_sync();
-        const uint32_t pb = p_addr + x * kTileBytes;
         const uint32_t vb = kv_addr + st * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          tc::mma_f16(tmem + kColO + x * kD, kmajor_desc(pb, kk), vmn_desc(vb, kk), kIdescO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // P columns: 16 keys = 8 packed columns
+          tc::mma_f16_ts(tmem + kColO + x * kD, tmem + x * kTileN + kk * 8, vmn_desc(vb, kk),
+                         kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         if (j == ntile - 1) tc::commit(&o_done[x]);
         return true;
       };
@@ -271,29 +269,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntile = x ? ntile_b : ntile_a;
     const int rows = x ? rows_b : rows_a;
     const float sl2 = a.scale_log2;
-    uint8_t* prow = sP + x * kTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < ntile && ok; ++j) {
       if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
       const int kbase = j * kTileN;
       const bool diag = kbase + kTileN - 1 > pos0;  // some key here is past some row
-      // pass 1: row max of the raw scores (scale > 0 keeps the order)
+      // Row max: the whole S row in one tensor-memory round trip (4 loads, one
+      // wait); keys past this row's position are skipped on diagonal tiles.
       float mx[8];
+      {
+        uint32_t r[4][32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::ld_32x32(t_s + c * 32, r);
+        for (int c = 0; c < 4; ++c) tc::ld_32x32(t_s + c * 32, r[c]);
         tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
         if (diag) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kbase + c * 32 + i <= pos) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (kbase + c * 32 + i <= pos) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
         }
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -319,38 +321,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::wait_st();
       }
-      // pass 2: P = 2^(s * scale * log2e - m) in fp16, row sum
+      // P = 2^(s * scale * log2e - m) in fp16, row sum: S reloaded 32 columns
+      // at a time, P stored over the first 64 columns of S_X.
       const float neg_m = -m;
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 packed columns per store
         uint32_t r[32];
         tc::ld_32x32(t_s + c * 32, r);
         tc::wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte chunks of 8 keys
-          uint32_t pk4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = q8 * 8 + 2 * e;
-            float p0 = ex2_approx(fmaf(__uint_as_float(r[i0]), sl2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(r[i0 + 1]), sl2, neg_m));
-            if (diag) {
-              if (kbase + c * 32 + i0 > pos) p0 = 0.f;
-              if (kbase + c * 32 + i0 + 1 > pos) p1 = 0.f;
-            }
-            rs[e] += p0 + p1;
-            __half2 hp = __floats2half2_rn(p0, p1);
-            pk4[e] = *reinterpret_cast<uint32_t*>(&hp);
+        for (int e = 0; e < 16; ++e) {
+          const int i0 = 2 * e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[i0]), sl2, neg_m));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[i0 + 1]), sl2, neg_m));
+          if (diag) {
+            if (kbase + c * 32 + i0 > pos) p0 = 0.f;
+            if (kbase + c * 32 + i0 + 1 > pos) p1 = 0.f;
           }
-          const int c16 = c * 4 + q8;  // chunk index 0..15 along the keys
-          const int slab = c16 >> 3, cc = c16 & 7;
-          *reinterpret_cast<uint4*>(prow + slab * kSlabBytes + ((cc ^ (row & 7)) << 4)) =
-              make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
+          rs[e & 3] += p0 + p1;
+          __half2 hp = __floats2half2_rn(p0, p1);
+          pk[e] = *reinterpret_cast<uint32_t*>(&hp);
         }
+        // P columns [16c, 16c+16) lie below S columns [32c, ...) not yet read.
+        tc::st_32x16(t_s + c * 16, pk);
       }
+      tc::wait_st();
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
       tc::fence_before_sync();
       mbar_arrive(&p_full[x]);
     }
