@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 512 << 20
 # partition kernel (the dominant kernel) from an ncu capture of this bench's
 # 38-sequence batch, keyed by the hash of the decode source it was taken on;
 # null once the source changes.
-DECODE_TRAFFIC = {"550f896f0f934f59": 852442624 + 5792512}
+DECODE_TRAFFIC = {"daf7868254c8f915": 852519680 + 5841920}
 
 
 def src_hash(name):
@@ -75,9 +75,9 @@ def write_bytes(T, H, D):
     return 2 * (2 * T * H * D * 2) + T * 8
 
 
-def make_workload(device, seed=1):
+def make_workload(device, seed=1, block_size=16):
     from paged_kv_cache_172_gb300 import workloads
-    return workloads.llama13b_decode(seed=seed, device=device)
+    return workloads.llama13b_decode(seed=seed, device=device, block_size=block_size)
 
 
 # ---------------------------------------------------------------------------
@@ -150,7 +150,7 @@ def run_gpu(args, rank, world, local_rank):
     build_lib.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    batch = make_workload(dev, seed=1 + rank)
+    batch = make_workload(dev, seed=1 + rank, block_size=args.block_size)
     B, H, D, bs = batch.B, batch.H, batch.D, batch.block_size
     ctx = batch.context_lens.cpu().numpy()
     max_ctx = 2048
@@ -338,9 +338,10 @@ def run_reference(args):
 
 def workload_config(batch, pt, l2):
     ctx = batch.context_lens.cpu().numpy()
-    return {"workload": "llama13b_decode_b38: 38 seqs x 40 heads x head_dim 128, block_size "
-                        "16, context_lens U[128,2048] (seed 1), pool 1.2x need, randomly "
-                        "permuted blocks; step = kv_cache_write of 38 new tokens + pa_decode",
+    return {"workload": f"llama13b_decode_b38: 38 seqs x 40 heads x head_dim 128, block_size "
+                        f"{batch.block_size}, context_lens U[128,2048] (seed 1), pool 1.2x "
+                        "need, randomly permuted blocks; step = kv_cache_write of 38 new tokens "
+                        "+ pa_decode",
             "B": int(batch.B), "H": int(batch.H), "head_dim": int(batch.D),
             "block_size": int(batch.block_size), "num_blocks": int(batch.num_blocks),
             "sum_context_len": int(ctx.sum()), "partition_tokens": pt, "l2": l2}
@@ -408,7 +409,7 @@ def run_aux(args, name):
                 "tails U[1,512], 40 heads, head_dim 128, block_size 16; step = block_copy of "
                 "128 copy-on-write blocks + pa_decode; GB/s on unique bytes")
     elif name == "long_context":
-        batch = workloads.long_context(seed=3, device=dev)
+        batch = workloads.long_context(seed=3, device=dev, bs=args.block_size)
         n = int(batch.context_lens[0])
         out = torch.empty_like(batch.q)
         H, D, bs = batch.H, batch.D, batch.block_size
@@ -418,10 +419,10 @@ def run_aux(args, name):
                                                   stream=stream))]
         work = decode_bytes([n], 1, H, D, bs)
         main, unit, bound, extra = "decode", "GB/s", "hbm", {}
-        desc = ("long_context_1M: 1 sequence of 1,048,576 tokens, 40 heads, head_dim 128, "
-                "block_size 16, 65,536 permuted blocks; split-KV decode")
+        desc = (f"long_context_1M: 1 sequence of 1,048,576 tokens, 40 heads, head_dim 128, "
+                f"block_size {bs}, {batch.num_blocks} permuted blocks; split-KV decode")
     elif name == "chunked_prefill":
-        batch = workloads.chunked_prefill(seed=4, device=dev)
+        batch = workloads.chunked_prefill(seed=4, device=dev, block_size=args.block_size)
         ctx = batch.context_lens.cpu().numpy()
         out = torch.empty_like(batch.q)
         B, H, Lq, D = batch.q.shape
@@ -440,8 +441,8 @@ def run_aux(args, name):
         main, unit, bound = "prefill", "TFLOP/s", "tensor"
         extra = {"useful_flops": work,
                  "kv_bytes": int(ctx.sum()) * H * D * 4, "q_out_bytes": 2 * batch.q.numel() * 2}
-        desc = ("chunked_prefill_8x512_on_3584: 8 sequences, 512-query chunk on 3,584 cached "
-                "tokens (context 4,096), 40 heads, head_dim 128, block_size 16; step = "
+        desc = (f"chunked_prefill_8x512_on_3584: 8 sequences, 512-query chunk on 3,584 cached "
+                f"tokens (context 4,096), 40 heads, head_dim 128, block_size {bs}; step = "
                 "kv_cache_write of the 4,096 chunk tokens + pa_prefill_chunk")
     else:
         raise SystemExit(f"unknown workload {name}")
@@ -526,6 +527,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="physical block size of the synthetic pools (16 or 32)")
     ap.add_argument("--workload", default="llama13b_decode",
                     choices=["llama13b_decode", "prefix_sharing", "long_context",
                              "chunked_prefill"])

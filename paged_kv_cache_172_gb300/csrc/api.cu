@@ -162,9 +162,10 @@ pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_c
 
   const long long rows = (long long)num_blocks * block_size;
   CUtensorMap kmap, vmap;
-  cudaError_t e = pk::make_pool_map(&kmap, k_cache, rows, H, D, 1, block_size);
+  const int box_tokens = block_size < 16 ? block_size : 16;  // decode stage = 16-token box
+  cudaError_t e = pk::make_pool_map(&kmap, k_cache, rows, H, D, 1, box_tokens);
   if (e != cudaSuccess) return PA_ERR_INVALID;
-  e = pk::make_pool_map(&vmap, v_cache, rows, H, D, 1, block_size);
+  e = pk::make_pool_map(&vmap, v_cache, rows, H, D, 1, box_tokens);
   if (e != cudaSuccess) return PA_ERR_INVALID;
 
   pk::DecodeArgs a;

@@ -13,9 +13,9 @@
 //    sequences that share prompt blocks are scheduled together, so shared
 //    blocks are read from HBM once and served from L2 to the sharers.
 //  * Each warp runs its own NSTAGE-deep TMA pipeline: lane 0 issues one 3-D
-//    tensor load per block for K and one for V (box = block_size rows of one
-//    head, the rows being block_size tokens apart by H*D*2 bytes in the pool),
-//    completing on a per-stage mbarrier.  The block-table entries of the
+//    tensor load per stage for K and one for V (box = min(block_size, 16)
+//    token rows of one head, H*D*2 bytes apart in the pool; a 32-token block
+//    is two stages), completing on a per-stage mbarrier.  The block-table entries of the
 //    partition are loaded once, one per lane, so address generation never
 //    waits on a dependent global load.
 //  * Scores: lane l owns D/32 consecutive dims; every lane forms partial dot
@@ -91,9 +91,11 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
 template <int D, int BS, int WARPS, int NSTAGE>
 struct PartitionCfg {
   static constexpr int EPL = D / 32;                  // dims per lane
-  static constexpr int TILE_BYTES = BS * D * 2;       // one head's rows of one block
+  static constexpr int TB = BS < 16 ? BS : 16;        // tokens per TMA box / pipeline stage
+  static constexpr int SUB = BS / TB;                 // stages per physical block
+  static constexpr int TILE_BYTES = TB * D * 2;       // one head's rows of one stage
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
-  static constexpr int LANES_PER_TOKEN = 32 / BS;     // lanes sharing a score after the butterfly
+  static constexpr int LANES_PER_TOKEN = 32 / TB;     // lanes sharing a score after the butterfly
   static constexpr int SMEM_BYTES = WARPS * NSTAGE * STAGE_BYTES + WARPS * NSTAGE * 8;
 };
 
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(WARPS * 32)
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE>;
   constexpr int EPL = Cfg::EPL;
+  constexpr int TB = Cfg::TB;
+  constexpr int SUB = Cfg::SUB;
   constexpr int LPT = Cfg::LANES_PER_TOKEN;
   static_assert(BS >= 1 && BS <= 32 && (32 % BS) == 0, "block_size must divide 32");
 
@@ -132,6 +136,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int tok1 = min(ctx, tok0 + a.part_tokens);
   const int lb0 = tok0 / BS;
   const int nblk = (tok1 - tok0 + BS - 1) / BS;  // <= 32 by construction of part_tokens
+  const int nunit = (tok1 - tok0 + TB - 1) / TB; // pipeline stages (TB-token sub-blocks)
 
   // Block-table entries of this partition, one per lane.
   int phys = 0;
@@ -157,14 +162,16 @@ __global__ void __launch_bounds__(WARPS * 32)
   }
   __syncwarp();
 
-  // Prologue: fill the pipeline.
-  for (int i = 0; i < NSTAGE && i < nblk; ++i) {
-    const int pb = __shfl_sync(kFull, phys, i);
+  // Prologue: fill the pipeline.  Unit u is tokens [u*TB, u*TB+TB) of the
+  // partition: sub-block u % SUB of logical block lb0 + u / SUB.
+  for (int i = 0; i < NSTAGE && i < nunit; ++i) {
+    const int pb = __shfl_sync(kFull, phys, i / SUB);
     if (lane == 0) {
       uint8_t* st = wbase + i * Cfg::STAGE_BYTES;
+      const int row = pb * BS + (i % SUB) * TB;
       mbar_arrive_expect_tx(&bars[i], Cfg::STAGE_BYTES);
-      tma_load_3d(st, &kmap, 0, h, pb * BS, &bars[i]);
-      tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, pb * BS, &bars[i]);
+      tma_load_3d(st, &kmap, 0, h, row, &bars[i]);
+      tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, row, &bars[i]);
     }
   }
 
@@ -175,20 +182,20 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   const int my_tok = lane / LPT;  // token whose score this lane holds after the butterfly
   int i = 0;
-  for (; i < nblk; ++i) {
+  for (; i < nunit; ++i) {
     const int s = i % NSTAGE;
     const uint32_t parity = (i / NSTAGE) & 1;
     const bool got = mbar_wait(&bars[s], parity);
     if (!__all_sync(kFull, got)) break;
 
     const __half* ks = reinterpret_cast<const __half*>(wbase + s * Cfg::STAGE_BYTES);
-    const __half* vs = ks + BS * D;
-    const int valid = min(BS, tok1 - (lb0 + i) * BS);  // tokens of this block inside the partition
+    const __half* vs = ks + TB * D;
+    const int valid = min(TB, tok1 - (tok0 + i * TB));  // tokens of this unit inside the partition
 
     // Partial dot products of every token of the block.
-    float part_dot[BS];
+    float part_dot[TB];
 #pragma unroll
-    for (int t = 0; t < BS; ++t) {
+    for (int t = 0; t < TB; ++t) {
       LaneVec<EPL> kv;
       kv.load(ks + t * D + lane * EPL);
       float kf[EPL];
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     // Transposing butterfly: after round r, lanes keep half of the tokens.
 #pragma unroll
-    for (int cnt = BS, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+    for (int cnt = TB, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
       const bool upper = (lane & off) != 0;
 #pragma unroll
       for (int k = 0; k < cnt / 2; ++k) {
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
 #pragma unroll
-    for (int t = 0; t < BS; ++t) {
+    for (int t = 0; t < TB; ++t) {
       const float pt = __shfl_sync(kFull, pr, t * LPT);
       if (t < valid) {
         LaneVec<EPL> vv;
@@ -241,27 +248,28 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     m = m_new;
 
-    // Refill this stage with block i + NSTAGE.
+    // Refill this stage with unit i + NSTAGE.
     __syncwarp();
     const int nxt = i + NSTAGE;
-    if (nxt < nblk) {
-      const int pb = __shfl_sync(kFull, phys, nxt);
+    if (nxt < nunit) {
+      const int pb = __shfl_sync(kFull, phys, nxt / SUB);
       if (lane == 0) {
         uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
+        const int row = pb * BS + (nxt % SUB) * TB;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[s], Cfg::STAGE_BYTES);
-        tma_load_3d(st, &kmap, 0, h, pb * BS, &bars[s]);
-        tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, pb * BS, &bars[s]);
+        tma_load_3d(st, &kmap, 0, h, row, &bars[s]);
+        tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, row, &bars[s]);
       }
     }
   }
 
   pdl_launch_dependents();  // the combine kernel may be scheduled now
-  if (i < nblk) {
+  if (i < nunit) {
     // A bounded wait gave up: report, drain what is still in flight (again
     // bounded) so no copy lands after the CTA exits, and write nothing.
     if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
-    for (int j = i; j < nblk && j < i + NSTAGE; ++j) mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
+    for (int j = i; j < nunit && j < i + NSTAGE; ++j) mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
     return;
   }
 
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
 template <int D, int BS>
 struct DecodeTuning {
   static constexpr int WARPS = PK_DECODE_WARPS;
-  static constexpr int STAGE = 2 * BS * D * 2;
+  static constexpr int STAGE = 2 * (BS < 16 ? BS : 16) * D * 2;
 #ifdef PK_DECODE_NSTAGE
   static constexpr int NSTAGE = PK_DECODE_NSTAGE;
 #else

@@ -239,14 +239,14 @@ def llama13b_context_lens(seed: int = 1) -> np.ndarray:
     return rng.integers(128, 2048, size=38, endpoint=True)
 
 
-def llama13b_decode(seed: int = 1, device="cpu") -> PagedBatch:
-    """LLaMA-13B-shaped decode: B=38, H=40, D=128, block_size=16, context
-    lengths uniform in [128, 2048] (inclusive, counting the new token),
-    pool sized ceil(1.2 x total blocks), one new token per sequence written
-    at position ctx-1 before decode."""
+def llama13b_decode(seed: int = 1, device="cpu", block_size: int = 16) -> PagedBatch:
+    """LLaMA-13B-shaped decode: B=38, H=40, D=128, block_size=16 (or the
+    given one), context lengths uniform in [128, 2048] (inclusive, counting
+    the new token), pool sized ceil(1.2 x total blocks), one new token per
+    sequence written at position ctx-1 before decode."""
     ctx = llama13b_context_lens(seed)
-    return random_decode(38, 40, 128, 16, ctx, seed, device=device,
-                         max_blocks=2048 // 16, new_tokens=True,
+    return random_decode(38, 40, 128, block_size, ctx, seed, device=device,
+                         max_blocks=2048 // block_size, new_tokens=True,
                          name="llama13b_decode_b38")
 
 
@@ -347,9 +347,9 @@ def long_context(seed: int = 3, device="cpu", context_len: int = 1 << 20,
                       meta={"seed": seed, "free_order": free_order})
 
 
-def chunked_prefill(seed: int = 4, device="cpu") -> PagedBatch:
+def chunked_prefill(seed: int = 4, device="cpu", block_size: int = 16) -> PagedBatch:
     """8 sequences, each a 512-query chunk appended to 3,584 cached tokens
     (context 4,096 = 256 blocks of 16), H=40, D=128; the chunk's K/V are
     written into the cache before attention."""
-    return random_prefill(8, 40, 128, 16, 512, [4096] * 8, seed, device=device,
+    return random_prefill(8, 40, 128, block_size, 512, [4096] * 8, seed, device=device,
                           name="chunked_prefill_8x512_on_3584")

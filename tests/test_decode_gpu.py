@@ -270,3 +270,19 @@ def test_long_context_1m():
     g["v_cache"].fill_(1.0)
     out1 = run_decode(g, batch.scale, n)
     assert torch.all(out1 == 1.0)
+
+
+def test_llama13b_batch_block32():
+    """The same 38-sequence batch laid out in 32-token blocks (decode stages
+    stream each block as two 16-token boxes)."""
+    batch = workloads.llama13b_decode(seed=1, device=DEV, block_size=32)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out = run_decode(g, batch.scale, 2048, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.arange(0, 38, 3)
+    ref = oracle.decode(batch.q.cpu().numpy()[sel], batch.k_cache.cpu().numpy(),
+                        batch.v_cache.cpu().numpy(), batch.block_tables.cpu().numpy()[sel],
+                        batch.context_lens.cpu().numpy()[sel], batch.scale)
+    assert_close(out[torch.from_numpy(sel).to(DEV)], ref, what="llama13b bs=32")
