@@ -1,7 +1,9 @@
 """Benchmark of the paged-decode hot path on GB300.
 
-One step = pa_kv_cache_write of the batch's new tokens + pa_decode (split
-partitions + log-sum-exp combine) over the LLaMA-13B-shaped batch: 38
+One step = the cache write of the batch's 38 new tokens fused into paged
+decode (pa_decode_append: split partitions + log-sum-exp combine; the
+two-launch path pa_kv_cache_write + pa_decode is timed beside it) over the
+LLaMA-13B-shaped batch: 38
 sequences, 40 heads, head_dim 128, block_size 16, context lengths uniform in
 [128, 2048], fp16 N(0,1) synthetic data.  The metric is algorithmic HBM
 GB/s (K+V rows attended + q + out + table/length reads + the cache write's
@@ -41,7 +43,7 @@ L2_FLUSH_BYTES = 512 << 20
 # partition kernel (the dominant kernel) from an ncu capture of this bench's
 # 38-sequence batch, keyed by the hash of the decode source it was taken on;
 # null once the source changes.
-DECODE_TRAFFIC = {"daf7868254c8f915": 852519680 + 5841920}
+DECODE_TRAFFIC = {"d78d7027021f588f": 853276416 + 6334976}
 
 
 def src_hash(name):
@@ -169,14 +171,23 @@ def run_gpu(args, rank, world, local_rank):
         torch.sum(flush, dim=0, out=flush_sink)
 
     def step():
+        # the 38 new tokens' cache write fused into the decode launch
+        pk.pa_decode_append(batch.q, batch.k_new, batch.v_new, batch.k_cache, batch.v_cache,
+                            batch.block_tables, batch.context_lens, batch.scale, max_ctx,
+                            out=out, partition_tokens=pt, workspace=ws, status=status,
+                            stream=stream)
+
+    def write_unfused():
         pk.pa_kv_cache_write(batch.k_new, batch.v_new, batch.slot_mapping, batch.k_cache,
                              batch.v_cache, status=status, stream=stream)
+
+    def decode_unfused():
         pk.pa_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
                      batch.context_lens, batch.scale, max_ctx, out=out, partition_tokens=pt,
                      workspace=ws, status=status, stream=stream)
 
     n_parts = -(-max_ctx // pt)
-    launches_per_step = 1 + 1 + (1 if n_parts > 1 else 0)
+    launches_per_step = 1 + (1 if n_parts > 1 else 0)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush_l2()
@@ -186,7 +197,7 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(status.item()):#x} during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -194,24 +205,31 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             for i in range(K):
                 flush_l2()  # evict the previous step from L2 (untimed)
-                e0, e1, e2 = ev[i]
-                e0.record(stream)
-                pk.pa_kv_cache_write(batch.k_new, batch.v_new, batch.slot_mapping,
-                                     batch.k_cache, batch.v_cache, status=status, stream=stream)
-                e1.record(stream)
-                pk.pa_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
-                             batch.context_lens, batch.scale, max_ctx, out=out,
-                             partition_tokens=pt, workspace=ws, status=status, stream=stream)
-                e2.record(stream)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    wr_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x} in the timed region")
     total_ms = sum(step_ms)
+
+    # -- the same step as two launches (cache write, then decode), for reference
+    uev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_l2()
+            uev[i][0].record(stream)
+            write_unfused()
+            uev[i][1].record(stream)
+            decode_unfused()
+            uev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    dec_ms = [uev[i][1].elapsed_time(uev[i][2]) for i in range(K)]
+    wr_ms = [uev[i][0].elapsed_time(uev[i][1]) for i in range(K)]
+    unfused_ms = [uev[i][0].elapsed_time(uev[i][2]) for i in range(K)]
 
     # -- end to end: host buffers, copies inside the timed region ---------------
     sess = DecodeSession(batch.k_cache, batch.v_cache, B, batch.block_tables.shape[1], max_ctx,
@@ -220,7 +238,6 @@ def run_gpu(args, rank, world, local_rank):
     host["q"].copy_(batch.q)
     host["k_new"].copy_(batch.k_new)
     host["v_new"].copy_(batch.v_new)
-    host["slots"].copy_(batch.slot_mapping)
     host["context_lens"].copy_(batch.context_lens)
     host["block_tables"].copy_(batch.block_tables)
     with torch.cuda.stream(stream):
@@ -244,8 +261,10 @@ def run_gpu(args, rank, world, local_rank):
     dbytes = decode_bytes(ctx, B, H, D, bs)
     sbytes = dbytes + write_bytes(int(batch.slot_mapping.numel()), H, D)
     res = {
-        "step_ms": total_ms / K, "decode_ms": statistics.mean(dec_ms),
+        "step_ms": total_ms / K, "step_ms_median": statistics.median(step_ms),
+        "decode_ms": statistics.mean(dec_ms),
         "decode_ms_median": statistics.median(dec_ms), "write_ms": statistics.mean(wr_ms),
+        "unfused_ms": statistics.mean(unfused_ms),
         "e2e_ms": e2e_ms / K, "step_bytes": sbytes, "decode_bytes": dbytes,
         "tokens": int(ctx.sum()), "clocks": clocks.summary(), "partition_tokens": pt,
         "num_parts": n_parts, "launches": launches_per_step * K,
@@ -340,8 +359,8 @@ def workload_config(batch, pt, l2):
     ctx = batch.context_lens.cpu().numpy()
     return {"workload": f"llama13b_decode_b38: 38 seqs x 40 heads x head_dim 128, block_size "
                         f"{batch.block_size}, context_lens U[128,2048] (seed 1), pool 1.2x "
-                        "need, randomly permuted blocks; step = kv_cache_write of 38 new tokens "
-                        "+ pa_decode",
+                        "need, randomly permuted blocks; step = cache write of 38 new tokens "
+                        "fused into decode (pa_decode_append)",
             "B": int(batch.B), "H": int(batch.H), "head_dim": int(batch.D),
             "block_size": int(batch.block_size), "num_blocks": int(batch.num_blocks),
             "sum_context_len": int(ctx.sum()), "partition_tokens": pt, "l2": l2}
@@ -562,7 +581,8 @@ def main():
 
     peak, peak_kind = measured_peak()
     value = all_bytes * K / total_s / 1e9
-    achieved = res["decode_bytes"] / dec_s / 1e9
+    # the step is one pa_decode_append call: its algorithmic bytes over its duration
+    achieved = step_bytes / (res["step_ms"] / 1e3) / 1e9
     key = src_hash("decode.cu")
     traffic = DECODE_TRAFFIC.get(key)
     batch = res["batch"]
@@ -575,14 +595,18 @@ def main():
                                   "flushed before every timed step (512 MB read, untimed)"),
         "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
         f"frac_of_{peak_kind}_hbm": value / peak,
-        "attended_tokens_per_s": res["tokens"] * world / (dec_s),
-        "decode_ms": res["decode_ms"], "decode_ms_median": res["decode_ms_median"],
-        "write_ms": res["write_ms"],
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (partition + combine kernels)",
+        "attended_tokens_per_s": res["tokens"] * world / (res["step_ms"] / 1e3),
+        "step_ms_median": res["step_ms_median"],
+        "two_launch_path": {"ms_per_step": res["unfused_ms"], "write_ms": res["write_ms"],
+                            "decode_ms": res["decode_ms"],
+                            "decode_GBs": res["decode_bytes"] / dec_s / 1e9},
+        "roofline": {"bound": "hbm",
+                     "kernel": "pa_decode_append (partition kernel with the fused cache write, "
+                               "+ combine kernel)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": traffic, "traffic_kernel": "partition_kernel",
-                     "algorithmic_bytes": res["decode_bytes"]},
+                     "algorithmic_bytes": step_bytes},
         "e2e": {"value": all_bytes * K / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": e2e_s / K * 1e3},

@@ -125,6 +125,31 @@ pa_status pa_decode(const pa_half *q, const pa_half *k_cache,
                     int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode with append: cache write of the new token fused into decode.
+ *
+ * Each decode step appends one token per sequence (tutorial "Block管理策略": the
+ * cache grows into the sequence's mapped blocks) and attends with it.  For
+ * every sequence b with n = context_lens[b] >= 1, the new token sits at
+ * position n-1: its K/V rows k_new[b], v_new[b] ([B, H, D] fp16) are stored
+ * to slot block_tables[b][(n-1)/bs] * bs + (n-1) % bs of k_cache/v_cache
+ * (bit-exact, as pa_kv_cache_write would), and the query attends to keys
+ * 0..n-1 exactly as pa_decode, the new key included.  One launch replaces
+ * pa_kv_cache_write + pa_decode.  Every other argument, the workspace and
+ * the errors are as for pa_decode; a block id outside [0, num_blocks) for
+ * the new token's block skips its store and sets PA_DEV_BAD_BLOCK_ID.
+ * k_new and v_new must not alias the caches.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_append(const pa_half *q, const pa_half *k_new,
+                           const pa_half *v_new, pa_half *k_cache,
+                           pa_half *v_cache, const int32_t *block_tables,
+                           const int32_t *context_lens, int B, int H, int D,
+                           int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len,
+                           int partition_tokens, float scale, pa_half *out,
+                           void *workspace, size_t workspace_bytes,
+                           int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode attention with no workspace and no allocation.
  *
  * This entry point has no counterpart on the pages; it exists for callers

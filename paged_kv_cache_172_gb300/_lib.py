@@ -24,6 +24,7 @@ EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
     "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy", "pa_decode_static",
+    "pa_decode_append",
 )
 
 # Size of the fixed scratch array behind pa_decode_static (PA_DECODE_STATIC_SCRATCH_BYTES).
@@ -66,6 +67,9 @@ def _bind(lib):
     lib.pa_decode_static.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _P, _P, _P]
     lib.pa_decode_static.restype = _I
+    lib.pa_decode_append.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _P, _P, _SZ, _P, _P]
+    lib.pa_decode_append.restype = _I
     return lib
 
 
@@ -156,6 +160,41 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_contex
                          int(max_context_len), int(partition_tokens), float(scale), _ptr(out),
                          _ptr(workspace), ws_len, _ptr(status), _stream(stream, q.device))
     _check(rc, "pa_decode")
+    return out
+
+
+def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                     max_context_len, out=None, partition_tokens=0, workspace=None, status=None,
+                     stream=None):
+    """Store each sequence's new token k_new/v_new [B,H,D] at position ctx-1
+    of the paged cache and run decode attention including it (one launch).
+    Returns ``out`` [B,H,D] fp16."""
+    _need(q, torch.float16, "q", 3)
+    _need(k_new, torch.float16, "k_new", 3)
+    _need(v_new, torch.float16, "v_new", 3)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    if k_new.shape != q.shape or v_new.shape != q.shape:
+        raise ValueError("k_new/v_new must be [B, H, D] like q")
+    if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
+                                        partition_tokens)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_tables), _ptr(context_lens), B, H, D, bs, NB,
+                                block_tables.shape[1], int(max_context_len),
+                                int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
+                                ws_len, _ptr(status), _stream(stream, q.device))
+    _check(rc, "pa_decode_append")
     return out
 
 

@@ -134,11 +134,14 @@ size_t pa_decode_workspace_size(int B, int H, int D, int block_size, int max_con
   return (size_t)B * H * parts * (size_t)(D + 2) * sizeof(float);
 }
 
-pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
-                    const int32_t* block_tables, const int32_t* context_lens, int B, int H, int D,
-                    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
-                    int partition_tokens, float scale, pa_half* out, void* workspace,
-                    size_t workspace_bytes, int32_t* status, pa_stream_t stream) {
+// Shared body of pa_decode and pa_decode_append (k_new/v_new null = no append).
+static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_half* v_new,
+                             const pa_half* k_cache, const pa_half* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, int B,
+                             int H, int D, int block_size, int num_blocks,
+                             int max_blocks_per_seq, int max_context_len, int partition_tokens,
+                             float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+                             int32_t* status, pa_stream_t stream) {
   if (B < 0 || H <= 0 || H > 65535 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
       !isfinite(scale))
     return PA_ERR_INVALID;
@@ -148,6 +151,8 @@ pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_c
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID;
   if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
   if ((long long)max_context_len > (long long)max_blocks_per_seq * block_size)
     return PA_ERR_INVALID;
@@ -170,6 +175,10 @@ pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_c
 
   pk::DecodeArgs a;
   a.q = reinterpret_cast<const __half*>(q);
+  a.k_new = reinterpret_cast<const __half*>(k_new);
+  a.v_new = reinterpret_cast<const __half*>(v_new);
+  a.k_cache = reinterpret_cast<__half*>(const_cast<pa_half*>(k_cache));
+  a.v_cache = reinterpret_cast<__half*>(const_cast<pa_half*>(v_cache));
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = reinterpret_cast<__half*>(out);
@@ -189,6 +198,28 @@ pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_c
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   e = pk::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int B, int H, int D,
+                    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
+                    int partition_tokens, float scale, pa_half* out, void* workspace,
+                    size_t workspace_bytes, int32_t* status, pa_stream_t stream) {
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, B, H, D,
+                     block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     partition_tokens, scale, out, workspace, workspace_bytes, status, stream);
+}
+
+pa_status pa_decode_append(const pa_half* q, const pa_half* k_new, const pa_half* v_new,
+                           pa_half* k_cache, pa_half* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int B, int H, int D, int block_size,
+                           int num_blocks, int max_blocks_per_seq, int max_context_len,
+                           int partition_tokens, float scale, pa_half* out, void* workspace,
+                           size_t workspace_bytes, int32_t* status, pa_stream_t stream) {
+  if (B > 0 && (!k_new || !v_new)) return PA_ERR_INVALID;
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B, H, D,
+                     block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     partition_tokens, scale, out, workspace, workspace_bytes, status, stream);
 }
 
 // ---------------------------------------------------------------------------

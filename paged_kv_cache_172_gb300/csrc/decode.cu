@@ -26,6 +26,11 @@
 //    instead of 5 per token.
 //  * Online softmax in the log2 domain (scale * log2(e) folded into one
 //    multiply), fp32 accumulation of P V with the lane's D/32 dims.
+//  * Optional append (pa_decode_append): the warp whose partition holds
+//    position ctx-1 stores the new token's K/V (its head's slice) to the
+//    cache slot the block table gives and scores it from registers-to-smem,
+//    so the cache write and the attention are one launch.  No other warp
+//    reads that slot.
 //  * A sequence that fits in one partition writes fp16 output directly;
 //    otherwise each partition writes (max, normaliser, unnormalised output)
 //    to the workspace and combine_kernel merges them by log-sum-exp.
@@ -188,9 +193,31 @@ __global__ void __launch_bounds__(WARPS * 32)
     const bool got = mbar_wait(&bars[s], parity);
     if (!__all_sync(kFull, got)) break;
 
-    const __half* ks = reinterpret_cast<const __half*>(wbase + s * Cfg::STAGE_BYTES);
-    const __half* vs = ks + TB * D;
+    __half* ks = reinterpret_cast<__half*>(wbase + s * Cfg::STAGE_BYTES);
+    __half* vs = ks + TB * D;
     const int valid = min(TB, tok1 - (tok0 + i * TB));  // tokens of this unit inside the partition
+
+    // Appending: the new token (position ctx-1) is scored from k_new/v_new,
+    // copied over the stage row TMA brought in, and stored to its cache slot.
+    if (a.k_new != nullptr) {
+      const int t_new = ctx - 1 - (tok0 + i * TB);
+      if (t_new >= 0 && t_new < TB) {
+        const int pb = __shfl_sync(kFull, phys, i / SUB);
+        const size_t src = row_bh * D + lane * EPL;
+        LaneVec<EPL> kn, vn;
+        kn.load(a.k_new + src);
+        vn.load(a.v_new + src);
+        *reinterpret_cast<decltype(kn.raw)*>(ks + t_new * D + lane * EPL) = kn.raw;
+        *reinterpret_cast<decltype(vn.raw)*>(vs + t_new * D + lane * EPL) = vn.raw;
+        if (pb < a.num_blocks) {
+          const size_t slot = (size_t)pb * BS + (i % SUB) * TB + t_new;
+          const size_t dst = (slot * a.H + h) * D + lane * EPL;
+          *reinterpret_cast<decltype(kn.raw)*>(a.k_cache + dst) = kn.raw;
+          *reinterpret_cast<decltype(vn.raw)*>(a.v_cache + dst) = vn.raw;
+        }
+        __syncwarp();
+      }
+    }
 
     // Partial dot products of every token of the block.
     float part_dot[TB];

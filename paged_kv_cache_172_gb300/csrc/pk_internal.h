@@ -17,6 +17,10 @@ void record_cuda_error(cudaError_t e);
 
 struct DecodeArgs {
   const __half* q;
+  const __half* k_new;  // [B, H, D] token appended at position ctx-1, or null
+  const __half* v_new;
+  __half* k_cache;      // pools, written only when appending
+  __half* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
   __half* out;

@@ -1,11 +1,12 @@
 """Host-facing decode step: device-resident paged KV state, host I/O per step.
 
 A serving loop keeps the KV pool, block tables and workspace on the GPU and
-moves only each step's small inputs (queries, the new tokens' K/V, their
-slots, updated lengths and tables) and the attention output across PCIe /
-C2C.  ``DecodeSession.step_from_host`` does exactly that around the two
-library calls: host->device copies, pa_kv_cache_write, pa_decode,
-device->host copy of the output, all asynchronous on one stream.
+moves only each step's small inputs (queries, the new tokens' K/V, updated
+lengths and tables) and the attention output across the host link.  ``DecodeSession.step_from_host`` does exactly that around one
+library call: host->device copies, pa_decode_append (the new tokens' cache
+write fused into decode), device->host copy of the output, all asynchronous
+on one stream.  The new token of sequence b sits at position
+context_lens[b] - 1, so the step's slots follow from the block tables.
 """
 import torch
 
@@ -26,7 +27,6 @@ class DecodeSession:
         self.out = torch.empty_like(self.q)
         self.k_new = torch.empty((B, H, D), dtype=torch.float16, device=dev)
         self.v_new = torch.empty_like(self.k_new)
-        self.slots = torch.empty(B, dtype=torch.int64, device=dev)
         self.context_lens = torch.empty(B, dtype=torch.int32, device=dev)
         self.block_tables = torch.empty((B, max_blocks_per_seq), dtype=torch.int32, device=dev)
         ws = _lib.pa_decode_workspace_size(B, H, D, bs, self.max_context_len,
@@ -40,7 +40,6 @@ class DecodeSession:
             "q": torch.empty(self.q.shape, dtype=torch.float16, **pin),
             "k_new": torch.empty(self.k_new.shape, dtype=torch.float16, **pin),
             "v_new": torch.empty(self.v_new.shape, dtype=torch.float16, **pin),
-            "slots": torch.empty(self.slots.shape, dtype=torch.int64, **pin),
             "context_lens": torch.empty(self.context_lens.shape, dtype=torch.int32, **pin),
             "block_tables": torch.empty(self.block_tables.shape, dtype=torch.int32, **pin),
             "out": torch.empty(self.out.shape, dtype=torch.float16, **pin),
@@ -48,8 +47,7 @@ class DecodeSession:
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in
-                   (self.q, self.k_new, self.v_new, self.slots, self.context_lens,
-                    self.block_tables))
+                   (self.q, self.k_new, self.v_new, self.context_lens, self.block_tables))
 
     def d2h_bytes(self):
         return self.out.numel() * self.out.element_size()
@@ -58,14 +56,13 @@ class DecodeSession:
         """One decode step from pinned host buffers (see host_buffers()); the
         output lands in host['out'] when the stream reaches the end."""
         for name, dst in (("q", self.q), ("k_new", self.k_new), ("v_new", self.v_new),
-                          ("slots", self.slots), ("context_lens", self.context_lens),
+                          ("context_lens", self.context_lens),
                           ("block_tables", self.block_tables)):
             dst.copy_(host[name], non_blocking=True)
-        _lib.pa_kv_cache_write(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache,
-                               status=status, stream=stream)
-        _lib.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
-                       self.scale, self.max_context_len, out=self.out,
-                       partition_tokens=self.partition_tokens, workspace=self.workspace,
-                       status=status, stream=stream)
+        _lib.pa_decode_append(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                              self.block_tables, self.context_lens, self.scale,
+                              self.max_context_len, out=self.out,
+                              partition_tokens=self.partition_tokens, workspace=self.workspace,
+                              status=status, stream=stream)
         host["out"].copy_(self.out, non_blocking=True)
         return host["out"]
