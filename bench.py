@@ -403,6 +403,8 @@ def run_aux(args, name):
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
     peak_hbm, hbm_kind = measured_peak()
+    extra = {}
+    extra_fns = {}
     if name == "prefix_sharing":
         batch = workloads.prefix_sharing(seed=2, device=dev)
         lay = batch.meta["layout"]
@@ -410,15 +412,22 @@ def run_aux(args, name):
         max_ctx = int(ctx.max())
         out = torch.empty_like(batch.q)
         H, D, bs = batch.H, batch.D, batch.block_size
+        sg, off, seqs, pref = (torch.from_numpy(x).to(dev)
+                               for x in workloads.sharing_groups(lay))
+        max_prefix = int(pref.max())
+        pt = max_prefix // 3  # 336: three partitions cover the 1,008 shared tokens
         phases = [
             ("block_copy", lambda: pk.pa_block_copy(batch.k_cache, batch.v_cache,
                                                     batch.copy_pairs, status=status,
                                                     stream=stream)),
-            ("decode", lambda: pk.pa_decode(batch.q, batch.k_cache, batch.v_cache,
-                                            batch.block_tables, batch.context_lens,
-                                            batch.scale, max_ctx, out=out, status=status,
-                                            stream=stream)),
+            ("decode", lambda: pk.pa_decode_shared_prefix(
+                batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                batch.context_lens, sg, off, seqs, pref, batch.scale, max_ctx, 8, max_prefix,
+                out=out, partition_tokens=pt, status=status, stream=stream)),
         ]
+        extra_fns["decode_without_sharing"] = lambda: pk.pa_decode(
+            batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.context_lens,
+            batch.scale, max_ctx, out=out, status=status, stream=stream)
         logical = decode_bytes(ctx, batch.B, H, D, bs)
         unique = unique_kv_bytes(lay.tables, ctx, bs, H, D) + 2 * batch.B * H * D * 2
         copy_bytes = 2 * 2 * len(lay.pairs) * bs * H * D * 2
@@ -426,7 +435,8 @@ def run_aux(args, name):
         extra = {"logical_bytes": logical, "unique_bytes": unique, "copy_bytes": copy_bytes}
         desc = ("prefix_sharing_16x8: 16 prompts x 8 samples, 1024-token shared prompts, "
                 "tails U[1,512], 40 heads, head_dim 128, block_size 16; step = block_copy of "
-                "128 copy-on-write blocks + pa_decode; GB/s on unique bytes")
+                "128 copy-on-write blocks + pa_decode_shared_prefix (groups of 8 sharing "
+                "1,008 tokens, 336-token partitions); GB/s on unique bytes")
     elif name == "long_context":
         batch = workloads.long_context(seed=3, device=dev, bs=args.block_size)
         n = int(batch.context_lens[0])
@@ -437,7 +447,7 @@ def run_aux(args, name):
                                                   batch.scale, n, out=out, status=status,
                                                   stream=stream))]
         work = decode_bytes([n], 1, H, D, bs)
-        main, unit, bound, extra = "decode", "GB/s", "hbm", {}
+        main, unit, bound = "decode", "GB/s", "hbm"
         desc = (f"long_context_1M: 1 sequence of 1,048,576 tokens, 40 heads, head_dim 128, "
                 f"block_size {bs}, {batch.num_blocks} permuted blocks; split-KV decode")
     elif name == "chunked_prefill":
@@ -492,6 +502,21 @@ def run_aux(args, name):
         raise RuntimeError(f"device status {int(status.item()):#x}")
     phase_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                 for i, (nm, _) in enumerate(phases)}
+    for nm, fn in extra_fns.items():  # alternatives timed beside the step, same flushing
+        xs = []
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+            for _ in range(K):
+                torch.sum(flush, dim=0, out=flush_sink)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                xs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        extra[f"{nm}_ms"] = statistics.mean(a.elapsed_time(b) for a, b in xs)
     step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
     main_s = phase_ms[main] / 1e3
     if bound == "tensor":

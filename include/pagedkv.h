@@ -125,6 +125,45 @@ pa_status pa_decode(const pa_half *q, const pa_half *k_cache,
                     int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode for groups of sequences that share a prefix of physical blocks.
+ *
+ * Sequences forked from one prompt point at the same physical blocks until
+ * they diverge (study notes "4. PagedAttention 带来的核心红利": shared blocks,
+ * copy-on-write).  Same result as pa_decode (same arguments, workspace and
+ * errors), but every partition of partition_tokens keys that lies entirely
+ * inside a group's shared prefix is read from HBM once for the whole group
+ * and attended by all its members' queries together; the remaining
+ * partitions run per sequence, and all are merged by log-sum-exp.
+ *
+ * Groups (CSR): members of group g are group_seqs[group_offsets[g] ..
+ * group_offsets[g+1]) (sequence indices, at most max_group_size <= 16 per
+ * group); group_prefix_len[g] is the number of leading tokens whose blocks
+ * all its members share; seq_group[b] is the group of sequence b or -1.  The
+ * caller guarantees that members' block tables agree on the shared blocks
+ * (the first member's table is read for them) and that every member's
+ * context holds the prefix.  max_prefix_len bounds group_prefix_len on the
+ * host.  Only whole partitions are shared: choose partition_tokens dividing
+ * the shared prefix for the full benefit.  D in {64, 128}, block_size in
+ * {16, 32}; other sizes return PA_ERR_UNSUPPORTED when num_groups > 0.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_shared_prefix(const pa_half *q, const pa_half *k_cache,
+                                  const pa_half *v_cache,
+                                  const int32_t *block_tables,
+                                  const int32_t *context_lens,
+                                  const int32_t *seq_group,
+                                  const int32_t *group_offsets,
+                                  const int32_t *group_seqs,
+                                  const int32_t *group_prefix_len,
+                                  int num_groups, int max_group_size,
+                                  int max_prefix_len, int B, int H, int D,
+                                  int block_size, int num_blocks,
+                                  int max_blocks_per_seq, int max_context_len,
+                                  int partition_tokens, float scale,
+                                  pa_half *out, void *workspace,
+                                  size_t workspace_bytes, int32_t *status,
+                                  pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode with append: cache write of the new token fused into decode.
  *
  * Each decode step appends one token per sequence (tutorial "Block管理策略": the

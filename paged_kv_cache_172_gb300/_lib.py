@@ -24,7 +24,7 @@ EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
     "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy", "pa_decode_static",
-    "pa_decode_append",
+    "pa_decode_append", "pa_decode_shared_prefix",
 )
 
 # Size of the fixed scratch array behind pa_decode_static (PA_DECODE_STATIC_SCRATCH_BYTES).
@@ -70,6 +70,10 @@ def _bind(lib):
     lib.pa_decode_append.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _P, _P, _SZ, _P, _P]
     lib.pa_decode_append.restype = _I
+    lib.pa_decode_shared_prefix.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                            _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                                            _SZ, _P, _P]
+    lib.pa_decode_shared_prefix.restype = _I
     return lib
 
 
@@ -195,6 +199,43 @@ def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_le
                                 int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
                                 ws_len, _ptr(status), _stream(stream, q.device))
     _check(rc, "pa_decode_append")
+    return out
+
+
+def pa_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, seq_group,
+                            group_offsets, group_seqs, group_prefix_len, scale, max_context_len,
+                            max_group_size, max_prefix_len, out=None, partition_tokens=0,
+                            workspace=None, status=None, stream=None):
+    """Decode where groups of sequences share prefix blocks (CSR groups:
+    members group_seqs[group_offsets[g]:group_offsets[g+1]], shared tokens
+    group_prefix_len[g], seq_group[b] = group or -1; all int32 on device).
+    Same result as pa_decode; shared partitions are read once per group."""
+    _need(q, torch.float16, "q", 3)
+    _need(k_cache, torch.float16, "k_cache", 4)
+    _need(v_cache, torch.float16, "v_cache", 4)
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("seq_group", seq_group), ("group_offsets", group_offsets),
+                    ("group_seqs", group_seqs), ("group_prefix_len", group_prefix_len)):
+        _need(t, torch.int32, name)
+    B, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    G = group_prefix_len.numel()
+    if group_offsets.numel() != G + 1 or seq_group.numel() != B:
+        raise ValueError("group_offsets must have G+1 entries and seq_group B entries")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
+                                        partition_tokens)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_shared_prefix(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(seq_group), _ptr(group_offsets), _ptr(group_seqs), _ptr(group_prefix_len), G,
+        int(max_group_size), int(max_prefix_len), B, H, D, bs, NB, block_tables.shape[1],
+        int(max_context_len), int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
+        ws_len, _ptr(status), _stream(stream, q.device))
+    _check(rc, "pa_decode_shared_prefix")
     return out
 
 

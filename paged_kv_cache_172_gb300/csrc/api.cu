@@ -134,14 +134,25 @@ size_t pa_decode_workspace_size(int B, int H, int D, int block_size, int max_con
   return (size_t)B * H * parts * (size_t)(D + 2) * sizeof(float);
 }
 
-// Shared body of pa_decode and pa_decode_append (k_new/v_new null = no append).
+// Optional shared-prefix description for decode_impl.
+struct PrefixGroups {
+  const int32_t* seq_group = nullptr;
+  const int32_t* group_offsets = nullptr;
+  const int32_t* group_seqs = nullptr;
+  const int32_t* group_prefix_len = nullptr;
+  int num_groups = 0, max_group_size = 0, max_prefix_len = 0;
+};
+
+// Shared body of pa_decode, pa_decode_append (k_new/v_new non-null) and
+// pa_decode_shared_prefix (groups non-null).
 static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_half* v_new,
                              const pa_half* k_cache, const pa_half* v_cache,
                              const int32_t* block_tables, const int32_t* context_lens, int B,
                              int H, int D, int block_size, int num_blocks,
                              int max_blocks_per_seq, int max_context_len, int partition_tokens,
                              float scale, pa_half* out, void* workspace, size_t workspace_bytes,
-                             int32_t* status, pa_stream_t stream) {
+                             int32_t* status, pa_stream_t stream,
+                             const PrefixGroups* groups = nullptr) {
   if (B < 0 || H <= 0 || H > 65535 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
       !isfinite(scale))
     return PA_ERR_INVALID;
@@ -164,6 +175,16 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   const size_t need = pa_decode_workspace_size(B, H, D, block_size, max_context_len, pt);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
   if (need > 0 && !aligned16(workspace)) return PA_ERR_INVALID;
+  int prefix_parts = 0;
+  if (groups != nullptr && groups->num_groups > 0) {
+    if (!groups->seq_group || !groups->group_offsets || !groups->group_seqs ||
+        !groups->group_prefix_len || groups->max_prefix_len < 0 ||
+        groups->max_prefix_len > max_context_len || groups->num_groups > 2147483647)
+      return PA_ERR_INVALID;
+    if (!pk::prefix_supported(D, block_size, groups->max_group_size)) return PA_ERR_UNSUPPORTED;
+    prefix_parts = groups->max_prefix_len / pt;
+    if (prefix_parts > 65535) return PA_ERR_INVALID;
+  }
 
   const long long rows = (long long)num_blocks * block_size;
   CUtensorMap kmap, vmap;
@@ -196,6 +217,34 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   a.part_tokens = pt;
   a.num_parts = (int)parts;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.seq_group = nullptr;
+  a.group_prefix_len = nullptr;
+  a.group_offsets = nullptr;
+  a.group_seqs = nullptr;
+  a.num_groups = 0;
+  a.max_group_size = 0;
+  a.max_prefix_parts = 0;
+  if (prefix_parts > 0) {
+    a.seq_group = groups->seq_group;
+    a.group_prefix_len = groups->group_prefix_len;
+    a.group_offsets = groups->group_offsets;
+    a.group_seqs = groups->group_seqs;
+    a.num_groups = groups->num_groups;
+    a.max_group_size = groups->max_group_size;
+    a.max_prefix_parts = prefix_parts;
+    // 64-dim halves in 128-byte swizzle for the prefix kernel's ldmatrix reads
+    CUtensorMap ksw, vsw;
+    const unsigned long long dims[3] = {(unsigned long long)D, (unsigned long long)H,
+                                        (unsigned long long)rows};
+    const unsigned long long strides[2] = {(unsigned long long)D * 2,
+                                           (unsigned long long)H * D * 2};
+    const unsigned box[3] = {64, 1, 16};
+    if (pk::make_map_3d(&ksw, k_cache, dims, strides, box, true) != cudaSuccess ||
+        pk::make_map_3d(&vsw, v_cache, dims, strides, box, true) != cudaSuccess)
+      return PA_ERR_INVALID;
+    e = pk::launch_prefix(a, ksw, vsw, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   e = pk::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -208,6 +257,31 @@ pa_status pa_decode(const pa_half* q, const pa_half* k_cache, const pa_half* v_c
   return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, B, H, D,
                      block_size, num_blocks, max_blocks_per_seq, max_context_len,
                      partition_tokens, scale, out, workspace, workspace_bytes, status, stream);
+}
+
+pa_status pa_decode_shared_prefix(const pa_half* q, const pa_half* k_cache,
+                                  const pa_half* v_cache, const int32_t* block_tables,
+                                  const int32_t* context_lens, const int32_t* seq_group,
+                                  const int32_t* group_offsets, const int32_t* group_seqs,
+                                  const int32_t* group_prefix_len, int num_groups,
+                                  int max_group_size, int max_prefix_len, int B, int H, int D,
+                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                  int max_context_len, int partition_tokens, float scale,
+                                  pa_half* out, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, pa_stream_t stream) {
+  if (num_groups < 0) return PA_ERR_INVALID;
+  PrefixGroups g;
+  g.seq_group = seq_group;
+  g.group_offsets = group_offsets;
+  g.group_seqs = group_seqs;
+  g.group_prefix_len = group_prefix_len;
+  g.num_groups = num_groups;
+  g.max_group_size = max_group_size;
+  g.max_prefix_len = max_prefix_len;
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens, B, H, D,
+                     block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     partition_tokens, scale, out, workspace, workspace_bytes, status, stream,
+                     &g);
 }
 
 pa_status pa_decode_append(const pa_half* q, const pa_half* k_new, const pa_half* v_new,

@@ -131,6 +131,13 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
   const int tok0 = part * a.part_tokens;
   const size_t row_bh = (size_t)b * a.H + h;
+  if (a.seq_group != nullptr) {  // partitions inside the group's shared prefix: prefix kernel
+    const int g = a.seq_group[b];
+    if (g >= 0 && g < a.num_groups) {
+      const int shared = min(a.group_prefix_len[g], ctx) / a.part_tokens * a.part_tokens;
+      if (tok0 + a.part_tokens <= shared) return;
+    }
+  }
   if (tok0 >= ctx) {
     if (part == 0) {  // empty sequence: zero row
       float z[EPL] = {};

@@ -30,6 +30,14 @@ struct DecodeArgs {
   int B, H, D, block_size, num_blocks, max_blocks, max_context_len;
   int part_tokens, num_parts;
   float scale_log2;  // scale * log2(e)
+  // Shared-prefix decode (null otherwise): group of each sequence (-1: none),
+  // and per group the tokens its members share; partitions lying entirely
+  // inside the shared prefix are computed once per group by the prefix kernel.
+  const int32_t* seq_group;
+  const int32_t* group_prefix_len;
+  const int32_t* group_offsets;  // [G+1] into group_seqs
+  const int32_t* group_seqs;     // member sequence indices, the first one's table is read
+  int num_groups, max_group_size, max_prefix_parts;
 };
 
 // Encodes the [num_blocks * block_size, H, D] view of a cache pool as a 3-D
@@ -48,6 +56,12 @@ cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 bool decode_supported(int D, int block_size);
+bool prefix_supported(int D, int block_size, int max_group_size);
+
+// Multi-query partials of the shared-prefix partitions (launched before
+// launch_decode when a.seq_group is set).
+cudaError_t launch_prefix(const DecodeArgs& a, const CUtensorMap& kmap_sw,
+                          const CUtensorMap& vmap_sw, cudaStream_t stream);
 
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
                                   int H, int D, long long n_slots, __half* kc, __half* vc,

@@ -40,6 +40,7 @@ __all__ = [
     "PagedBatch", "TinySchedule", "tiny_schedule", "llama13b_decode",
     "prefix_sharing", "prefix_sharing_layout", "SharingLayout",
     "llama13b_context_lens", "long_context", "chunked_prefill", "random_decode",
+    "sharing_groups",
     "random_prefill", "shuffled_pool", "fill_tables",
 ]
 
@@ -307,6 +308,20 @@ def prefix_sharing_layout(seed: int = 2, prompts: int = 16, samples: int = 8,
     ctx = (prompt_len + tails).astype(np.int32)
     return SharingLayout(NB, tables, ctx, np.asarray(pairs, dtype=np.int64),
                          free_order, prompt_blocks, tails, P, S, prompt_len, bs)
+
+
+def sharing_groups(lay: "SharingLayout"):
+    """CSR description of the prefix-sharing layout's groups: the samples of
+    prompt p form group p; they share the prompt's blocks 0..n-2 (the last
+    prompt block is each sample's private copy).  Returns numpy int32
+    (seq_group[B], group_offsets[G+1], group_seqs[B], group_prefix_len[G])."""
+    P, S = lay.prompts, lay.samples
+    seq_group = np.repeat(np.arange(P, dtype=np.int32), S)
+    offsets = (np.arange(P + 1, dtype=np.int32) * S).astype(np.int32)
+    seqs = np.arange(P * S, dtype=np.int32)
+    shared = lay.prompt_len - lay.block_size
+    prefix = np.full(P, shared, dtype=np.int32)
+    return seq_group, offsets, seqs, prefix
 
 
 def prefix_sharing(seed: int = 2, device="cpu", H: int = 40, D: int = 128,
