@@ -19,6 +19,9 @@ Functions and the passages they follow (page titles and sections):
   block_copy -- study notes "DataWhale组队学习笔记--llm-algo-leetcode(五)",
       "4. PagedAttention 带来的核心红利" (copy-on-write of shared blocks).
   gather -- the same notes, "代码实现" (get_physical_cache).
+  e4m3_* / kv_cache_write_fp8 / decode_fp8 -- the blog's sec. 2.3 "mixed
+      precision KV storage", read as e4m3 codes with one fp32 scale per
+      (token, head) row (scale = max|row| / 448); decode dequantizes exactly.
   allocator.BlockAllocator -- the same notes' KVCacheManager plus the
       tutorial's Free List / Allocator table.
 """
@@ -30,7 +33,8 @@ from . import build as _build
 
 __all__ = [
     "OracleError", "half_to_double", "attend_row", "decode", "prefill",
-    "kv_cache_write", "block_copy", "gather", "load",
+    "kv_cache_write", "block_copy", "gather", "load", "e4m3_to_double", "e4m3_from_float",
+    "kv_cache_write_fp8", "decode_fp8",
 ]
 
 _ERRORS = {
@@ -67,8 +71,16 @@ def _bind(lib):
                                           _P, _P]
     lib.oracle_block_copy.argtypes = [_P, _P, _P, i32, i32, i32, i32, i64]
     lib.oracle_gather.argtypes = [_P, _P, i32, i32, i32, i32, i32, i32, i64, _P]
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+    lib.oracle_kv_cache_write_fp8.argtypes = [_P, _P, _P, i32, i32, i32, i32, i64, _P, _P, _P, _P]
+    lib.oracle_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, i32, i32, i32, i32, i64, i32,
+                                      dbl, _P]
     for f in ("oracle_attend_row", "oracle_decode", "oracle_prefill",
-              "oracle_kv_cache_write", "oracle_block_copy", "oracle_gather"):
+              "oracle_kv_cache_write", "oracle_block_copy", "oracle_gather",
+              "oracle_kv_cache_write_fp8", "oracle_decode_fp8"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -189,4 +201,50 @@ def gather(pool, table, seq_len, head, lib=None):
     out = np.zeros((seq_len, D), dtype=np.float64)
     _check(lib.oracle_gather(_ptr(pb), _ptr(tb), int(tb.size), int(seq_len), H,
                              int(head), D, bs, nb, _ptr(out)))
+    return out
+
+
+def e4m3_to_double(code, lib=None):
+    lib = lib or load()
+    return lib.oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def e4m3_from_float(x, lib=None):
+    lib = lib or load()
+    return lib.oracle_e4m3_from_float(float(np.float32(x)))
+
+
+def kv_cache_write_fp8(k, v, slot_mapping, k8, v8, kscale, vscale, lib=None):
+    """Quantizing cache write.  k, v [T,H,D] fp16; k8/v8 [NB,bs,H,D] uint8;
+    kscale/vscale [NB,H,bs] float32.  Returns new (k8, v8, kscale, vscale)."""
+    lib = lib or load()
+    kb, vb = _bits(k), _bits(v)
+    T, H, D = kb.shape
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8).copy()
+    v8 = np.ascontiguousarray(v8, dtype=np.uint8).copy()
+    ks = np.ascontiguousarray(kscale, dtype=np.float32).copy()
+    vs = np.ascontiguousarray(vscale, dtype=np.float32).copy()
+    nb, bs = k8.shape[0], k8.shape[1]
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64).reshape(T)
+    _check(lib.oracle_kv_cache_write_fp8(_ptr(kb), _ptr(vb), _ptr(sm), T, H, D, bs, nb,
+                                         _ptr(k8), _ptr(v8), _ptr(ks), _ptr(vs)))
+    return k8, v8, ks, vs
+
+
+def decode_fp8(q, k8, v8, kscale, vscale, block_tables, context_lens, scale, lib=None):
+    """Decode over an e4m3 cache (exact dequantization): out[B,H,D] fp64."""
+    lib = lib or load()
+    qb = _bits(q)
+    B, H, D = qb.shape
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    v8 = np.ascontiguousarray(v8, dtype=np.uint8)
+    ks = np.ascontiguousarray(kscale, dtype=np.float32)
+    vs = np.ascontiguousarray(vscale, dtype=np.float32)
+    nb, bs = k8.shape[0], k8.shape[1]
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32).reshape(B, -1)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32).reshape(B)
+    out = np.zeros((B, H, D), dtype=np.float64)
+    _check(lib.oracle_decode_fp8(_ptr(qb), _ptr(k8), _ptr(v8), _ptr(ks), _ptr(vs), _ptr(bt),
+                                 _ptr(cl), B, H, D, bs, nb, bt.shape[1], float(scale),
+                                 _ptr(out)))
     return out

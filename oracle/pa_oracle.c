@@ -291,3 +291,173 @@ int oracle_gather(const uint16_t *pool, const int32_t *table, int table_len,
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 (e4m3) KV storage -- the "mixed-precision KV storage" of the blog
+ * "PagedAttention origin and evolution", sec. 2.3, read as: each (token,
+ * head) row of K and of V is stored as D e4m3 codes plus one fp32 scale,
+ * value = code * scale, scale = max|row| / 448 (448 is the largest finite
+ * e4m3 value), a zero row gets scale 1.
+ *
+ * e4m3 ("fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits, no infinities; S.1111.111 is NaN; the largest finite value is
+ * S.1111.110 = 1.75 * 2^8 = 448; exponent 0 is subnormal: frac * 2^-9.
+ * ------------------------------------------------------------------------ */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int frac = c & 7;
+    double mag;
+    if (e == 15 && frac == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)frac, -9);
+    else
+        mag = ldexp((double)(8 + frac), e - 10);
+    return sign ? -mag : mag;
+}
+
+/* Round a float to the nearest e4m3 value, ties to even, saturating to
+ * +-448.  Works on the exact binary value of x: every e4m3 value is exactly
+ * representable in double, so the nearest one is found by comparing
+ * distances to the two neighbours below and above |x|. */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    if (x != x)
+        return 0x7f;
+    int sign = signbit(x) ? 1 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)((sign << 7) | 0x7e);
+    /* largest code whose magnitude is <= a */
+    int lo = 0;
+    for (int c = 0; c <= 0x7e; ++c)
+        if (oracle_e4m3_to_double((uint8_t)c) <= a)
+            lo = c;
+    int hi = lo < 0x7e ? lo + 1 : lo;
+    double dlo = a - oracle_e4m3_to_double((uint8_t)lo);
+    double dhi = oracle_e4m3_to_double((uint8_t)hi) - a;
+    int pick;
+    if (dlo < dhi)
+        pick = lo;
+    else if (dhi < dlo)
+        pick = hi;
+    else
+        pick = (lo & 1) ? hi : lo; /* tie: even fraction (last bit 0) */
+    return (uint8_t)((sign << 7) | pick);
+}
+
+/* Quantizing cache write: like oracle_kv_cache_write, but each (token, head)
+ * row is stored as e4m3 codes into k8/v8 [num_blocks, bs, H, D] with its
+ * fp32 scale in ks/vs [num_blocks, H, bs].  The scale and the quotient are
+ * IEEE single-precision divisions. */
+static void quantize_row(const uint16_t *x, int D, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float v = (float)fabs(oracle_half_to_double(x[d]));
+        if (v > amax)
+            amax = v;
+    }
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int d = 0; d < D; ++d) {
+        float v = (float)oracle_half_to_double(x[d]);
+        codes[d] = oracle_e4m3_from_float(v / s);
+    }
+    *scale = s;
+}
+
+int oracle_kv_cache_write_fp8(const uint16_t *k, const uint16_t *v,
+                              const int64_t *slot_mapping, int T, int H, int D,
+                              int bs, int64_t num_blocks, uint8_t *k8,
+                              uint8_t *v8, float *ks, float *vs)
+{
+    if (T < 0 || H <= 0 || D <= 0 || bs <= 0)
+        return ORACLE_BAD_ARG;
+    int64_t n_slots = num_blocks * bs;
+    for (int t = 0; t < T; ++t) {
+        if (slot_mapping[t] >= n_slots)
+            return ORACLE_BAD_SLOT;
+        for (int u = 0; u < t; ++u)
+            if (slot_mapping[t] >= 0 && slot_mapping[u] == slot_mapping[t])
+                return ORACLE_DUP_SLOT;
+    }
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t blk = slot / bs, off = slot % bs;
+        for (int h = 0; h < H; ++h) {
+            int64_t src = ((int64_t)t * H + h) * D;
+            int64_t dst = (slot * H + h) * D;
+            int64_t si = (blk * H + h) * bs + off;
+            quantize_row(k + src, D, k8 + dst, ks + si);
+            quantize_row(v + src, D, v8 + dst, vs + si);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode over an e4m3 cache: key j of head h is e4m3(k8[...]) * ks[...],
+ * dequantized exactly in double; then the same definition as
+ * oracle_attend_row. */
+int oracle_decode_fp8(const uint16_t *q, const uint8_t *k8, const uint8_t *v8,
+                      const float *ks, const float *vs,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int B, int H, int D, int bs, int64_t num_blocks,
+                      int max_blocks_per_seq, double scale, double *out)
+{
+    if (B < 0 || H <= 0 || D <= 0 || bs <= 0 || max_blocks_per_seq < 0)
+        return ORACLE_BAD_ARG;
+    for (int b = 0; b < B; ++b) {
+        int n = context_lens[b];
+        const int32_t *table = block_tables + (int64_t)b * max_blocks_per_seq;
+        if (n < 0 || (int64_t)n > (int64_t)max_blocks_per_seq * bs)
+            return ORACLE_BAD_CONTEXT;
+        for (int lb = 0; lb < (n + bs - 1) / bs; ++lb)
+            if (table[lb] < 0 || (int64_t)table[lb] >= num_blocks)
+                return ORACLE_BAD_BLOCK;
+        for (int h = 0; h < H; ++h) {
+            double *o = out + ((int64_t)b * H + h) * D;
+            for (int d = 0; d < D; ++d)
+                o[d] = 0.0;
+            if (n == 0)
+                continue;
+            double *s = (double *)malloc(sizeof(double) * (size_t)n);
+            if (!s)
+                return ORACLE_BAD_ARG;
+            const uint16_t *qr = q + ((int64_t)b * H + h) * D;
+            for (int j = 0; j < n; ++j) {
+                int64_t blk = table[j / bs];
+                int off = j % bs;
+                const uint8_t *kr = k8 + ((blk * bs + off) * H + h) * D;
+                double kscale = (double)ks[(blk * H + h) * bs + off];
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += oracle_half_to_double(qr[d]) * (oracle_e4m3_to_double(kr[d]) * kscale);
+                s[j] = scale * dot;
+            }
+            double m = s[0];
+            for (int j = 1; j < n; ++j)
+                if (s[j] > m)
+                    m = s[j];
+            double z = 0.0;
+            for (int j = 0; j < n; ++j) {
+                s[j] = exp(s[j] - m);
+                z += s[j];
+            }
+            for (int j = 0; j < n; ++j) {
+                int64_t blk = table[j / bs];
+                int off = j % bs;
+                const uint8_t *vr = v8 + ((blk * bs + off) * H + h) * D;
+                double vscale = (double)vs[(blk * H + h) * bs + off];
+                double w = s[j] / z;
+                for (int d = 0; d < D; ++d)
+                    o[d] += w * (oracle_e4m3_to_double(vr[d]) * vscale);
+            }
+            free(s);
+        }
+    }
+    return ORACLE_OK;
+}

@@ -316,13 +316,120 @@ def check_block_copy(lib):
     assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
 
 
+# ---- FP8 (e4m3) storage -------------------------------------------------------
+E4M3_KNOWN = {0x00: 0.0, 0x38: 1.0, 0x30: 0.5, 0x7E: 448.0, 0x01: 2.0 ** -9,
+              0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x39: 1.125, 0x3F: 1.875,
+              0xB8: -1.0, 0xFE: -448.0, 0x40: 2.0}
+
+
+def check_e4m3_decode(lib):
+    for code, val in E4M3_KNOWN.items():
+        assert oracle.e4m3_to_double(code, lib=lib) == val, hex(code)
+    assert math.isnan(oracle.e4m3_to_double(0x7F, lib=lib))
+    assert math.isnan(oracle.e4m3_to_double(0xFF, lib=lib))
+    import torch
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c, lib=lib) for c in range(256)])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin]) and np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def check_e4m3_encode(lib):
+    # every finite code round-trips
+    for c in range(256):
+        v = oracle.e4m3_to_double(c, lib=lib)
+        if math.isfinite(v):
+            got = oracle.e4m3_from_float(v, lib=lib)
+            assert got == c or (v == 0.0 and got in (0x00, 0x80)), (hex(c), hex(got))
+    # ties go to the even code; just past a tie goes up; saturation at 448
+    assert oracle.e4m3_from_float(1.0625, lib=lib) == 0x38
+    assert oracle.e4m3_from_float(1.1875, lib=lib) == 0x3A
+    assert oracle.e4m3_from_float(np.nextafter(np.float32(1.0625), np.float32(2)), lib=lib) == 0x39
+    assert oracle.e4m3_from_float(1000.0, lib=lib) == 0x7E
+    assert oracle.e4m3_from_float(-1000.0, lib=lib) == 0xFE
+    # torch's float32 -> float8_e4m3fn (round to nearest even) on in-range values
+    import torch
+    x = np.random.default_rng(30).standard_normal(2000).astype(np.float32) * 50
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_float(v, lib=lib) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def _fp8_case(rng, nb=6, bs=4, H=2, D=16):
+    k8 = np.zeros((nb, bs, H, D), np.uint8)
+    v8 = np.zeros_like(k8)
+    ks = np.ones((nb, H, bs), np.float32)
+    vs = np.ones_like(ks)
+    return k8, v8, ks, vs
+
+
+def check_fp8_quantize(lib):
+    rng = np.random.default_rng(31)
+    k8, v8, ks, vs = _fp8_case(rng)
+    T, H, D = 5, 2, 16
+    k = rand16(rng, (T, H, D)) * np.float16(3)
+    v = rand16(rng, (T, H, D))
+    v[2, 1] = 0  # an all-zero row: scale 1, codes 0
+    slots = np.array([0, 5, 9, 23, -1], np.int64)
+    k8, v8, ks, vs = oracle.kv_cache_write_fp8(k, v, slots, k8, v8, ks, vs, lib=lib)
+    bs = 4
+    for t, sl in enumerate(slots[:4]):
+        blk, off = sl // bs, sl % bs
+        for h in range(H):
+            for x, codes, sc in ((k[t, h], k8[blk, off, h], ks[blk, h, off]),
+                                 (v[t, h], v8[blk, off, h], vs[blk, h, off])):
+                xf = x.astype(np.float32)
+                amax = np.float32(np.abs(xf).max())
+                assert sc == (amax / np.float32(448) if amax > 0 else 1.0)
+                dec = np.array([oracle.e4m3_to_double(c, lib=lib) for c in codes])
+                deq = dec * sc
+                if amax > 0:  # the max element maps to +-448; 448 * scale ~ max within 1 ulp
+                    assert np.max(np.abs(dec)) == 448.0
+                    assert abs(np.max(np.abs(deq)) - float(amax)) <= float(amax) * 2.0 ** -23
+                err = np.abs(deq - xf.astype(np.float64))
+                assert np.all(err <= np.abs(xf) * 2.0 ** -4 + 2.0 ** -10 * sc)
+    assert np.all(v8[9 // bs, 9 % bs, 1] == 0) and vs[9 // bs, 1, 9 % bs] == 1.0
+
+
+def check_fp8_decode_dense(lib):
+    rng = np.random.default_rng(32)
+    B, H, D, bs = 3, 2, 16, 4
+    ctx = [5, 9, 1]
+    nb = 8
+    k8 = rng.integers(0, 0x7E, size=(nb, bs, H, D), dtype=np.uint8) | \
+        (rng.integers(0, 2, size=(nb, bs, H, D), dtype=np.uint8) << 7)
+    v8 = rng.integers(0, 0x7E, size=(nb, bs, H, D), dtype=np.uint8)
+    ks = (rng.random((nb, H, bs)) * 0.01 + 0.001).astype(np.float32)
+    vs = (rng.random((nb, H, bs)) * 0.01 + 0.001).astype(np.float32)
+    perm = rng.permutation(nb)
+    tables = np.full((B, 3), -1, np.int32)
+    pos = 0
+    for b, c in enumerate(ctx):
+        n = -(-c // bs)
+        tables[b, :n] = perm[pos:pos + n]
+        pos += n
+    q = rand16(rng, (B, H, D))
+    out = oracle.decode_fp8(q, k8, v8, ks, vs, tables, ctx, 0.3, lib=lib)
+    dec = np.vectorize(lambda c: oracle.e4m3_to_double(int(c), lib=lib))
+    for b in range(B):
+        j = np.arange(ctx[b])
+        blk, off = tables[b, j // bs], j % bs
+        for h in range(H):
+            K = dec(k8[blk, off, h, :]) * ks[blk, h, off][:, None]
+            V = dec(v8[blk, off, h, :]) * vs[blk, h, off][:, None]
+            ref = dense_attention(q[b, h][None].astype(np.float64), K, V, 0.3)[0]
+            assert np.allclose(out[b, h], ref, rtol=1e-12, atol=1e-14)
+
+
 ALL_CHECKS = [
     check_half_known, check_half_all_patterns, check_worked_examples,
     check_closed_form_uniform, check_single_key_and_ones,
     check_two_keys_logistic, check_scale_zero_mean, check_dense_decode,
     check_dense_prefill, check_prefill_whole_context_is_tril,
     check_prefill_lq1_is_decode, check_permutation_invariance,
-    check_cache_write, check_block_copy,
+    check_cache_write, check_block_copy, check_e4m3_decode, check_e4m3_encode,
+    check_fp8_quantize, check_fp8_decode_dense,
 ]
 
 
@@ -441,19 +548,30 @@ def test_allocator_fork_cow():
 # mutation tests: each planted mistake must fail at least one pin
 # ----------------------------------------------------------------------------
 MUTANTS = {
-    "drop_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "drop_scale": ("pool_at(k_cache, blk, tok, head, d, bs, H, D);\n        s[j] = scale * dot;",
+                   "pool_at(k_cache, blk, tok, head, d, bs, H, D);\n        s[j] = dot;"),
     "token_index_swapped": ("int tok = j % bs;\n        double dot", "int tok = j / bs;\n        double dot"),
-    "no_normalisation": ("double w = s[j] / z;", "double w = s[j];"),
+    "no_normalisation": ("double w = s[j] / z;\n        for (int d = 0; d < D; ++d)\n            out[d]",
+                         "double w = s[j];\n        for (int d = 0; d < D; ++d)\n            out[d]"),
     "mask_off_by_one": ("ctx - Lq + i + 1", "ctx - Lq + i"),
     "head_row_swapped": ("(((blk * bs + tok) * (int64_t)H + head) * D) + d",
                          "(((blk * bs + head) * (int64_t)H + tok) * D) + d"),
     "exponent_bias": ("ldexp((double)(1024 + frac), e - 25)", "ldexp((double)(1024 + frac), e - 24)"),
     "subnormal_scale": ("ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
-    "max_not_subtracted_wrong_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
+    "max_not_subtracted_wrong_sign": ("        s[j] = exp(s[j] - m);\n        z += s[j];\n    }\n    /* weighted",
+                                      "        s[j] = exp(m - s[j]);\n        z += s[j];\n    }\n    /* weighted"),
+    "fp8_no_normalisation": ("double w = s[j] / z;\n                for",
+                             "double w = s[j];\n                for"),
     "write_wrong_pool": ("v_cache[slot * row + e] = v[(int64_t)t * row + e];",
                          "v_cache[slot * row + e] = k[(int64_t)t * row + e];"),
     "copy_reversed": ("memcpy(k_cache + dst * blk, k_cache + src * blk",
                       "memcpy(k_cache + src * blk, k_cache + dst * blk"),
+    "e4m3_bias": ("ldexp((double)(8 + frac), e - 10)", "ldexp((double)(8 + frac), e - 11)"),
+    "e4m3_tie_up": ("pick = (lo & 1) ? hi : lo;", "pick = hi;"),
+    "fp8_scale_index": ("double kscale = (double)ks[(blk * H + h) * bs + off];",
+                        "double kscale = (double)ks[(blk * bs + off) * H + h];"),
+    "fp8_scale_max": ("float s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                      "float s = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     "first_key_skipped": ("for (int j = 0; j < n_keys; ++j) {\n        int64_t blk = table[j / bs];\n        int tok = j % bs;\n        double w",
                           "for (int j = 1; j < n_keys; ++j) {\n        int64_t blk = table[j / bs];\n        int tok = j % bs;\n        double w"),
 }
