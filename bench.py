@@ -437,6 +437,38 @@ def run_aux(args, name):
                 "tails U[1,512], 40 heads, head_dim 128, block_size 16; step = block_copy of "
                 "128 copy-on-write blocks + pa_decode_shared_prefix (groups of 8 sharing "
                 "1,008 tokens, 336-token partitions); GB/s on unique bytes")
+    elif name == "llama13b_decode_fp8":
+        batch = make_workload(dev, seed=1, block_size=args.block_size)
+        NB, bs, H, D = batch.k_cache.shape
+        k8 = torch.zeros((NB, bs, H, D), dtype=torch.uint8, device=dev)
+        v8 = torch.zeros_like(k8)
+        ks = torch.ones((NB, H, bs), dtype=torch.float32, device=dev)
+        vs = torch.ones_like(ks)
+        all_slots = torch.arange(NB * bs, dtype=torch.int64, device=dev)
+        pk.pa_kv_cache_write_fp8(batch.k_cache.reshape(NB * bs, H, D),
+                                 batch.v_cache.reshape(NB * bs, H, D), all_slots, k8, v8, ks, vs,
+                                 status=status)  # quantize the whole pool once (untimed)
+        out = torch.empty_like(batch.q)
+        ctx = batch.context_lens.cpu().numpy()
+        T = int(batch.slot_mapping.numel())
+        phases = [
+            ("kv_cache_write_fp8", lambda: pk.pa_kv_cache_write_fp8(
+                batch.k_new, batch.v_new, batch.slot_mapping, k8, v8, ks, vs, status=status,
+                stream=stream)),
+            ("decode", lambda: pk.pa_decode_fp8(batch.q, k8, v8, ks, vs, batch.block_tables,
+                                                batch.context_lens, batch.scale, 2048, out=out,
+                                                status=status, stream=stream)),
+        ]
+        # e4m3 K and V rows (D bytes each) and their two fp32 scales, + q/out/tables
+        work = int(ctx.sum()) * H * (2 * D + 8) + 2 * batch.B * H * D * 2 + \
+            int(sum(-(-int(c) // bs) for c in ctx)) * 4 + batch.B * 4
+        main, unit, bound = "decode", "GB/s", "hbm"
+        extra = {"fp8_algorithmic_bytes": work,
+                 "fp16_equivalent_bytes": decode_bytes(ctx, batch.B, H, D, bs),
+                 "write_fp8_bytes": T * H * (2 * 2 * D + 2 * D + 8)}
+        desc = ("llama13b_decode_b38_fp8: the 38-sequence batch stored as e4m3 with "
+                "per-(token, head) fp32 scales; step = quantizing write of 38 new tokens + "
+                "pa_decode_fp8; GB/s on fp8 bytes")
     elif name == "long_context":
         batch = workloads.long_context(seed=3, device=dev, bs=args.block_size)
         n = int(batch.context_lens[0])
@@ -544,6 +576,8 @@ def run_aux(args, name):
     line.update(extra)
     if name == "prefix_sharing":
         line["logical_GBs"] = logical / main_s / 1e9
+    if name == "llama13b_decode_fp8":
+        line["attended_tokens_per_s"] = int(ctx.sum()) / main_s
     print(json.dumps(line))
 
 
@@ -575,7 +609,7 @@ def main():
                     help="physical block size of the synthetic pools (16 or 32)")
     ap.add_argument("--workload", default="llama13b_decode",
                     choices=["llama13b_decode", "prefix_sharing", "long_context",
-                             "chunked_prefill"])
+                             "chunked_prefill", "llama13b_decode_fp8"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -189,6 +189,40 @@ pa_status pa_decode_append(const pa_half *q, const pa_half *k_new,
                            int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 (e4m3) KV storage: quantizing cache write and decode over it.
+ *
+ * The blog's sec. 2.3 lists mixed-precision KV storage; this is its reading
+ * here.  Each (token, head) row of K and of V is stored as D e4m3 codes
+ * (1 sign, 4 exponent bits with bias 7, 3 fraction bits, largest finite
+ * value 448) plus one fp32 scale: value = code * scale, with
+ * scale = max|row| / 448 (1 for an all-zero row) and code = e4m3(x / scale)
+ * rounded to nearest even (both divisions correctly rounded fp32).  A row is
+ * D + 4 bytes instead of 2D, so decode reads about half the bytes.
+ *
+ * k_cache8, v_cache8  [num_blocks, block_size, H, D] uint8 (e4m3 codes)
+ * k_scale, v_scale    [num_blocks, H, block_size] float32
+ * pa_kv_cache_write_fp8 takes the same tokens and slots as
+ * pa_kv_cache_write (fp16 k, v [T, H, D]) and writes codes and scales.
+ * pa_decode_fp8 computes pa_decode's result on the dequantized cache
+ * (fp32 accumulation, fp16 output), same arguments, workspace and errors.
+ * ------------------------------------------------------------------------- */
+pa_status pa_kv_cache_write_fp8(const pa_half *k, const pa_half *v,
+                                const int64_t *slot_mapping, int T, int H,
+                                int D, int block_size, int num_blocks,
+                                uint8_t *k_cache8, uint8_t *v_cache8,
+                                float *k_scale, float *v_scale,
+                                int32_t *status, pa_stream_t stream);
+
+pa_status pa_decode_fp8(const pa_half *q, const uint8_t *k_cache8,
+                        const uint8_t *v_cache8, const float *k_scale,
+                        const float *v_scale, const int32_t *block_tables,
+                        const int32_t *context_lens, int B, int H, int D,
+                        int block_size, int num_blocks, int max_blocks_per_seq,
+                        int max_context_len, int partition_tokens, float scale,
+                        pa_half *out, void *workspace, size_t workspace_bytes,
+                        int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Decode attention with no workspace and no allocation.
  *
  * This entry point has no counterpart on the pages; it exists for callers

@@ -24,7 +24,7 @@ EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
     "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy", "pa_decode_static",
-    "pa_decode_append", "pa_decode_shared_prefix",
+    "pa_decode_append", "pa_decode_shared_prefix", "pa_kv_cache_write_fp8", "pa_decode_fp8",
 )
 
 # Size of the fixed scratch array behind pa_decode_static (PA_DECODE_STATIC_SCRATCH_BYTES).
@@ -74,6 +74,11 @@ def _bind(lib):
                                             _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
                                             _SZ, _P, _P]
     lib.pa_decode_shared_prefix.restype = _I
+    lib.pa_kv_cache_write_fp8.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+    lib.pa_kv_cache_write_fp8.restype = _I
+    lib.pa_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                  ctypes.c_float, _P, _P, _SZ, _P, _P]
+    lib.pa_decode_fp8.restype = _I
     return lib
 
 
@@ -236,6 +241,59 @@ def pa_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, seq
         int(max_context_len), int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
         ws_len, _ptr(status), _stream(stream, q.device))
     _check(rc, "pa_decode_shared_prefix")
+    return out
+
+
+def pa_kv_cache_write_fp8(k, v, slot_mapping, k_cache8, v_cache8, k_scale, v_scale, status=None,
+                          stream=None):
+    """Quantize k/v [T,H,D] fp16 into e4m3 pools k_cache8/v_cache8
+    [NB,bs,H,D] uint8 with per-(token, head) scales k_scale/v_scale
+    [NB,H,bs] float32, at slot_mapping [T] int64."""
+    _need(k, torch.float16, "k", 3)
+    _need(v, torch.float16, "v", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(k_cache8, torch.uint8, "k_cache8", 4)
+    _need(v_cache8, torch.uint8, "v_cache8", 4)
+    _need(k_scale, torch.float32, "k_scale", 3)
+    _need(v_scale, torch.float32, "v_scale", 3)
+    T, H, D = k.shape
+    NB, bs = k_cache8.shape[0], k_cache8.shape[1]
+    if tuple(k_scale.shape) != (NB, H, bs) or v_scale.shape != k_scale.shape:
+        raise ValueError("scales must be [num_blocks, H, block_size]")
+    rc = lib().pa_kv_cache_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, bs, NB,
+                                     _ptr(k_cache8), _ptr(v_cache8), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(status), _stream(stream, k.device))
+    _check(rc, "pa_kv_cache_write_fp8")
+
+
+def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_lens, scale,
+                  max_context_len, out=None, partition_tokens=0, workspace=None, status=None,
+                  stream=None):
+    """Paged decode over e4m3 pools with per-(token, head) scales."""
+    _need(q, torch.float16, "q", 3)
+    _need(k_cache8, torch.uint8, "k_cache8", 4)
+    _need(v_cache8, torch.uint8, "v_cache8", 4)
+    _need(k_scale, torch.float32, "k_scale", 3)
+    _need(v_scale, torch.float32, "v_scale", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    B, H, D = q.shape
+    NB, bs = k_cache8.shape[0], k_cache8.shape[1]
+    if tuple(k_cache8.shape) != (NB, bs, H, D) or v_cache8.shape != k_cache8.shape:
+        raise ValueError("fp8 pools must be [num_blocks, block_size, H, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
+                                        partition_tokens)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_fp8(_ptr(q), _ptr(k_cache8), _ptr(v_cache8), _ptr(k_scale),
+                             _ptr(v_scale), _ptr(block_tables), _ptr(context_lens), B, H, D, bs,
+                             NB, block_tables.shape[1], int(max_context_len),
+                             int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
+                             ws_len, _ptr(status), _stream(stream, q.device))
+    _check(rc, "pa_decode_fp8")
     return out
 
 

@@ -5,6 +5,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "pk_internal.h"
@@ -67,14 +69,14 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, in
 
 cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long long dims[3],
                         const unsigned long long strides[2], const unsigned box[3],
-                        bool swizzle128) {
+                        bool swizzle128, CUtensorMapDataType dtype) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
   cuuint64_t st[2] = {strides[0], strides[1]};
   cuuint32_t bx[3] = {box[0], box[1], box[2]};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), d, st, bx,
+  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, bx,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -143,8 +145,17 @@ struct PrefixGroups {
   int num_groups = 0, max_group_size = 0, max_prefix_len = 0;
 };
 
-// Shared body of pa_decode, pa_decode_append (k_new/v_new non-null) and
-// pa_decode_shared_prefix (groups non-null).
+// Optional FP8 (e4m3) pools with per-(token, head) scales [num_blocks, H, bs].
+struct Fp8Pools {
+  const uint8_t* k8 = nullptr;
+  const uint8_t* v8 = nullptr;
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
+};
+
+// Shared body of pa_decode, pa_decode_append (k_new/v_new non-null),
+// pa_decode_shared_prefix (groups non-null) and pa_decode_fp8 (fp8 non-null,
+// k_cache/v_cache then unused).
 static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_half* v_new,
                              const pa_half* k_cache, const pa_half* v_cache,
                              const int32_t* block_tables, const int32_t* context_lens, int B,
@@ -152,13 +163,23 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
                              int max_blocks_per_seq, int max_context_len, int partition_tokens,
                              float scale, pa_half* out, void* workspace, size_t workspace_bytes,
                              int32_t* status, pa_stream_t stream,
-                             const PrefixGroups* groups = nullptr) {
+                             const PrefixGroups* groups = nullptr,
+                             const Fp8Pools* fp8 = nullptr) {
   if (B < 0 || H <= 0 || H > 65535 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
       !isfinite(scale))
     return PA_ERR_INVALID;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
   if (B == 0) return PA_OK;
+  if (fp8 != nullptr) {
+    if (!fp8->k8 || !fp8->v8 || !fp8->k_scale || !fp8->v_scale || k_new) return PA_ERR_INVALID;
+    if (!aligned16(fp8->k8) || !aligned16(fp8->v8) || !aligned16(fp8->k_scale) ||
+        !aligned16(fp8->v_scale))
+      return PA_ERR_INVALID;
+    if (groups != nullptr) return PA_ERR_UNSUPPORTED;
+    k_cache = reinterpret_cast<const pa_half*>(fp8->k8);  // non-null placeholders below
+    v_cache = reinterpret_cast<const pa_half*>(fp8->v8);
+  }
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_INVALID;
@@ -187,11 +208,36 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   }
 
   const long long rows = (long long)num_blocks * block_size;
-  CUtensorMap kmap, vmap;
+  pk::DecodeMaps maps;
+  memset(&maps, 0, sizeof(maps));
   const int box_tokens = block_size < 16 ? block_size : 16;  // decode stage = 16-token box
-  cudaError_t e = pk::make_pool_map(&kmap, k_cache, rows, H, D, 1, box_tokens);
-  if (e != cudaSuccess) return PA_ERR_INVALID;
-  e = pk::make_pool_map(&vmap, v_cache, rows, H, D, 1, box_tokens);
+  cudaError_t e;
+  if (fp8 == nullptr) {
+    e = pk::make_pool_map(&maps.k, k_cache, rows, H, D, 1, box_tokens);
+    if (e == cudaSuccess) e = pk::make_pool_map(&maps.v, v_cache, rows, H, D, 1, box_tokens);
+  } else {
+    const unsigned long long dims[3] = {(unsigned long long)D, (unsigned long long)H,
+                                        (unsigned long long)rows};
+    const unsigned long long strides[2] = {(unsigned long long)D,
+                                           (unsigned long long)H * D};
+    const unsigned box[3] = {(unsigned)D, 1, (unsigned)box_tokens};
+    e = pk::make_map_3d(&maps.k, fp8->k8, dims, strides, box, false,
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (e == cudaSuccess)
+      e = pk::make_map_3d(&maps.v, fp8->v8, dims, strides, box, false,
+                          CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    const unsigned long long sdims[3] = {(unsigned long long)block_size, (unsigned long long)H,
+                                         (unsigned long long)num_blocks};
+    const unsigned long long sstrides[2] = {(unsigned long long)block_size * 4,
+                                            (unsigned long long)H * block_size * 4};
+    const unsigned sbox[3] = {(unsigned)box_tokens, 1, 1};
+    if (e == cudaSuccess)
+      e = pk::make_map_3d(&maps.ks, fp8->k_scale, sdims, sstrides, sbox, false,
+                          CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    if (e == cudaSuccess)
+      e = pk::make_map_3d(&maps.vs, fp8->v_scale, sdims, sstrides, sbox, false,
+                          CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+  }
   if (e != cudaSuccess) return PA_ERR_INVALID;
 
   pk::DecodeArgs a;
@@ -224,6 +270,9 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   a.num_groups = 0;
   a.max_group_size = 0;
   a.max_prefix_parts = 0;
+  a.fp8 = fp8 != nullptr;
+  a.k_scale = fp8 ? fp8->k_scale : nullptr;
+  a.v_scale = fp8 ? fp8->v_scale : nullptr;
   if (prefix_parts > 0) {
     a.seq_group = groups->seq_group;
     a.group_prefix_len = groups->group_prefix_len;
@@ -245,7 +294,7 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
     e = pk::launch_prefix(a, ksw, vsw, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  e = pk::launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  e = pk::launch_decode(a, maps, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
@@ -282,6 +331,45 @@ pa_status pa_decode_shared_prefix(const pa_half* q, const pa_half* k_cache,
                      block_size, num_blocks, max_blocks_per_seq, max_context_len,
                      partition_tokens, scale, out, workspace, workspace_bytes, status, stream,
                      &g);
+}
+
+pa_status pa_decode_fp8(const pa_half* q, const uint8_t* k_cache8, const uint8_t* v_cache8,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        const int32_t* context_lens, int B, int H, int D, int block_size,
+                        int num_blocks, int max_blocks_per_seq, int max_context_len,
+                        int partition_tokens, float scale, pa_half* out, void* workspace,
+                        size_t workspace_bytes, int32_t* status, pa_stream_t stream) {
+  Fp8Pools p;
+  p.k8 = k_cache8;
+  p.v8 = v_cache8;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  if (B > 0 && (!k_cache8 || !v_cache8 || !k_scale || !v_scale)) return PA_ERR_INVALID;
+  return decode_impl(q, nullptr, nullptr, nullptr, nullptr, block_tables, context_lens, B, H, D,
+                     block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     partition_tokens, scale, out, workspace, workspace_bytes, status, stream,
+                     nullptr, &p);
+}
+
+pa_status pa_kv_cache_write_fp8(const pa_half* k, const pa_half* v, const int64_t* slot_mapping,
+                                int T, int H, int D, int block_size, int num_blocks,
+                                uint8_t* k_cache8, uint8_t* v_cache8, float* k_scale,
+                                float* v_scale, int32_t* status, pa_stream_t stream) {
+  if (T < 0 || H <= 0 || D <= 0) return PA_ERR_INVALID;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (T == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache8 || !v_cache8 || !k_scale || !v_scale)
+    return PA_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache8) || !aligned16(v_cache8) ||
+      !aligned16(k_scale) || !aligned16(v_scale))
+    return PA_ERR_INVALID;
+  if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  cudaError_t e = pk::launch_kv_cache_write_fp8(
+      reinterpret_cast<const __half*>(k), reinterpret_cast<const __half*>(v), slot_mapping, T, H,
+      D, block_size, (long long)num_blocks * block_size, k_cache8, v_cache8, k_scale, v_scale,
+      status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
 pa_status pa_decode_append(const pa_half* q, const pa_half* k_new, const pa_half* v_new,

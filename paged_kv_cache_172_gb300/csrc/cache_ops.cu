@@ -13,6 +13,8 @@
 // in flight per thread before the stores, grid sized so every SM has many
 // CTAs.  Bounds are checked against the pool on the device; bad entries set
 // a status bit and are skipped.
+#include <cuda_fp8.h>
+
 #include "pk_common.cuh"
 #include "pk_internal.h"
 
@@ -93,7 +95,77 @@ __global__ void __launch_bounds__(kCopyThreads)
   copy_vectors(pool + src * block_vecs, pool + dst * block_vecs, begin, end);
 }
 
+// Quantizing write into e4m3 pools: one warp per (token, head) row; lane l
+// owns D/32 consecutive dims.  scale = max|row| / 448 (1 for a zero row),
+// code = e4m3(x / scale) rounded to nearest even (both divisions correctly
+// rounded single precision).  grid = (T, 2): K (0) or V (1).
+template <int D>
+__global__ void __launch_bounds__(kCopyThreads)
+    kv_cache_write_fp8_kernel(const __half* __restrict__ k, const __half* __restrict__ v,
+                              const int64_t* __restrict__ slots, int H, int bs, long long n_slots,
+                              uint8_t* __restrict__ k8, uint8_t* __restrict__ v8,
+                              float* __restrict__ ks, float* __restrict__ vs, int32_t* status) {
+  constexpr int EPL = D / 32;
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const long long slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= n_slots) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) flag_status(status, PA_DEV_BAD_SLOT);
+    return;
+  }
+  const long long blk = slot / bs, off = slot % bs;
+  const __half* src_pool = blockIdx.y == 0 ? k : v;
+  uint8_t* dst_pool = blockIdx.y == 0 ? k8 : v8;
+  float* scl = blockIdx.y == 0 ? ks : vs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int h = warp; h < H; h += kCopyThreads / 32) {
+    const __half* src = src_pool + ((long long)t * H + h) * D + lane * EPL;
+    float x[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(src + e));
+      x[e] = f.x;
+      x[e + 1] = f.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[e], sc), __NV_SATFINITE,
+                                                         __NV_E4M3);
+      packed |= (uint32_t)c << (8 * e);
+    }
+    uint8_t* dst = dst_pool + (slot * H + h) * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+    }
+    if (lane == 0) scl[(blk * H + h) * bs + off] = sc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_cache_write_fp8(const __half* k, const __half* v, const int64_t* slots,
+                                      int T, int H, int D, int block_size, long long n_slots,
+                                      uint8_t* k8, uint8_t* v8, float* k_scale, float* v_scale,
+                                      int32_t* status, cudaStream_t stream) {
+  dim3 grid(T, 2);
+  if (D == 128)
+    kv_cache_write_fp8_kernel<128><<<grid, kCopyThreads, 0, stream>>>(
+        k, v, slots, H, block_size, n_slots, k8, v8, k_scale, v_scale, status);
+  else
+    kv_cache_write_fp8_kernel<64><<<grid, kCopyThreads, 0, stream>>>(
+        k, v, slots, H, block_size, n_slots, k8, v8, k_scale, v_scale, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
                                   int H, int D, long long n_slots, __half* kc, __half* vc,

@@ -36,6 +36,8 @@
 //    to the workspace and combine_kernel merges them by log-sum-exp.
 #include <math.h>
 
+#include <cuda_fp8.h>
+
 #include "pk_common.cuh"
 #include "pk_internal.h"
 
@@ -67,6 +69,32 @@ struct LaneVec<2> {
   }
 };
 
+// EPL e4m3 codes of one lane (FP8 pools), decoded exactly to float.
+template <int EPL>
+struct LaneVec8;
+template <>
+struct LaneVec8<4> {
+  uint32_t raw;
+  __device__ __forceinline__ void load(const uint8_t* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ __forceinline__ void to_float(float* f) const {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+};
+template <>
+struct LaneVec8<2> {
+  uint16_t raw;
+  __device__ __forceinline__ void load(const uint8_t* p) { raw = *reinterpret_cast<const uint16_t*>(p); }
+  __device__ __forceinline__ void to_float(float* f) const {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)raw, __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    f[0] = a.x; f[1] = a.y;
+  }
+};
+
 template <int EPL>
 __device__ __forceinline__ void store_half_row(__half* dst, const float* v) {
   if constexpr (EPL == 4) {
@@ -93,22 +121,27 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
   return ctx;
 }
 
-template <int D, int BS, int WARPS, int NSTAGE>
+template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
 struct PartitionCfg {
   static constexpr int EPL = D / 32;                  // dims per lane
   static constexpr int TB = BS < 16 ? BS : 16;        // tokens per TMA box / pipeline stage
   static constexpr int SUB = BS / TB;                 // stages per physical block
-  static constexpr int TILE_BYTES = TB * D * 2;       // one head's rows of one stage
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile + V tile
+  static constexpr int ELEM = FP8 ? 1 : 2;            // bytes per stored K/V element
+  static constexpr int TILE_BYTES = TB * D * ELEM;    // one head's rows of one stage
+  static constexpr int SCALE_BYTES = FP8 ? TB * 4 : 0;  // per-token scales of one stage
+  static constexpr int SCALE_SLOT = FP8 ? 128 : 0;      // 128-byte aligned TMA destination
+  // stage = [K rows][V rows][K scales][V scales]; TX_BYTES actually land
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SCALE_SLOT;
+  static constexpr int TX_BYTES = 2 * TILE_BYTES + 2 * SCALE_BYTES;
+  static_assert(TILE_BYTES % 128 == 0 && STAGE_BYTES % 128 == 0, "TMA destinations 128-B aligned");
   static constexpr int LANES_PER_TOKEN = 32 / TB;     // lanes sharing a score after the butterfly
   static constexpr int SMEM_BYTES = WARPS * NSTAGE * STAGE_BYTES + WARPS * NSTAGE * 8;
 };
 
-template <int D, int BS, int WARPS, int NSTAGE>
+template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
 __global__ void __launch_bounds__(WARPS * 32)
-    partition_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE>;
+    partition_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
+  using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE, FP8>;
   constexpr int EPL = Cfg::EPL;
   constexpr int TB = Cfg::TB;
   constexpr int SUB = Cfg::SUB;
@@ -176,16 +209,22 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   // Prologue: fill the pipeline.  Unit u is tokens [u*TB, u*TB+TB) of the
   // partition: sub-block u % SUB of logical block lb0 + u / SUB.
-  for (int i = 0; i < NSTAGE && i < nunit; ++i) {
-    const int pb = __shfl_sync(kFull, phys, i / SUB);
+  auto issue = [&](int u, int s) {  // all lanes (shuffle), lane 0 issues
+    const int pb = __shfl_sync(kFull, phys, u / SUB);
     if (lane == 0) {
-      uint8_t* st = wbase + i * Cfg::STAGE_BYTES;
-      const int row = pb * BS + (i % SUB) * TB;
-      mbar_arrive_expect_tx(&bars[i], Cfg::STAGE_BYTES);
-      tma_load_3d(st, &kmap, 0, h, row, &bars[i]);
-      tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, row, &bars[i]);
+      uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
+      const int row = pb * BS + (u % SUB) * TB;
+      mbar_arrive_expect_tx(&bars[s], Cfg::TX_BYTES);
+      tma_load_3d(st, &maps.k, 0, h, row, &bars[s]);
+      tma_load_3d(st + Cfg::TILE_BYTES, &maps.v, 0, h, row, &bars[s]);
+      if constexpr (FP8) {  // scales [num_blocks, H, bs]: box of TB tokens
+        tma_load_3d(st + 2 * Cfg::TILE_BYTES, &maps.ks, (u % SUB) * TB, h, pb, &bars[s]);
+        tma_load_3d(st + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT, &maps.vs, (u % SUB) * TB, h, pb,
+                    &bars[s]);
+      }
     }
-  }
+  };
+  for (int i = 0; i < NSTAGE && i < nunit; ++i) issue(i, i);
 
   float m = -INFINITY, l = 0.f;
   float o[EPL];
@@ -200,13 +239,16 @@ __global__ void __launch_bounds__(WARPS * 32)
     const bool got = mbar_wait(&bars[s], parity);
     if (!__all_sync(kFull, got)) break;
 
-    __half* ks = reinterpret_cast<__half*>(wbase + s * Cfg::STAGE_BYTES);
-    __half* vs = ks + TB * D;
+    uint8_t* kst = wbase + s * Cfg::STAGE_BYTES;
+    __half* ks = reinterpret_cast<__half*>(kst);
+    __half* vs = reinterpret_cast<__half*>(kst + Cfg::TILE_BYTES);
+    const float* kscl = reinterpret_cast<const float*>(kst + 2 * Cfg::TILE_BYTES);
+    const float* vscl = reinterpret_cast<const float*>(kst + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT);
     const int valid = min(TB, tok1 - (tok0 + i * TB));  // tokens of this unit inside the partition
 
     // Appending: the new token (position ctx-1) is scored from k_new/v_new,
     // copied over the stage row TMA brought in, and stored to its cache slot.
-    if (a.k_new != nullptr) {
+    if (!FP8 && a.k_new != nullptr) {
       const int t_new = ctx - 1 - (tok0 + i * TB);
       if (t_new >= 0 && t_new < TB) {
         const int pb = __shfl_sync(kFull, phys, i / SUB);
@@ -230,10 +272,16 @@ __global__ void __launch_bounds__(WARPS * 32)
     float part_dot[TB];
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
-      LaneVec<EPL> kv;
-      kv.load(ks + t * D + lane * EPL);
       float kf[EPL];
-      kv.to_float(kf);
+      if constexpr (FP8) {
+        LaneVec8<EPL> kv;
+        kv.load(kst + t * D + lane * EPL);
+        kv.to_float(kf);
+      } else {
+        LaneVec<EPL> kv;
+        kv.load(ks + t * D + lane * EPL);
+        kv.to_float(kf);
+      }
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
@@ -255,7 +303,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int off = LPT / 2; off >= 1; off >>= 1)
       part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
 
-    float sc = (my_tok < valid) ? part_dot[0] * a.scale_log2 : -INFINITY;
+    float dot = part_dot[0];
+    if constexpr (FP8) dot *= kscl[my_tok];  // per-(token, head) dequantization scale
+    float sc = (my_tok < valid) ? dot * a.scale_log2 : -INFINITY;
     float mb = sc;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
@@ -270,12 +320,19 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
-      const float pt = __shfl_sync(kFull, pr, t * LPT);
+      float pt = __shfl_sync(kFull, pr, t * LPT);
       if (t < valid) {
-        LaneVec<EPL> vv;
-        vv.load(vs + t * D + lane * EPL);
         float vf[EPL];
-        vv.to_float(vf);
+        if constexpr (FP8) {
+          pt *= vscl[t];  // fold the V row's scale into its weight
+          LaneVec8<EPL> vv;
+          vv.load(kst + Cfg::TILE_BYTES + t * D + lane * EPL);
+          vv.to_float(vf);
+        } else {
+          LaneVec<EPL> vv;
+          vv.load(vs + t * D + lane * EPL);
+          vv.to_float(vf);
+        }
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
       }
@@ -286,15 +343,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     __syncwarp();
     const int nxt = i + NSTAGE;
     if (nxt < nunit) {
-      const int pb = __shfl_sync(kFull, phys, nxt / SUB);
-      if (lane == 0) {
-        uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
-        const int row = pb * BS + (nxt % SUB) * TB;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[s], Cfg::STAGE_BYTES);
-        tma_load_3d(st, &kmap, 0, h, row, &bars[s]);
-        tma_load_3d(st + Cfg::TILE_BYTES, &vmap, 0, h, row, &bars[s]);
-      }
+      if (lane == 0) fence_proxy_async_smem();
+      issue(nxt, s);
     }
   }
 
@@ -413,16 +463,22 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
 #define PK_DECODE_INFLIGHT_BYTES 16384
 #endif
 
-template <int D, int BS>
+#ifndef PK_DECODE_FP8_NSTAGE
+#define PK_DECODE_FP8_NSTAGE 3
+#endif
+
+template <int D, int BS, bool FP8>
 struct DecodeTuning {
   static constexpr int WARPS = PK_DECODE_WARPS;
   static constexpr int STAGE = 2 * (BS < 16 ? BS : 16) * D * 2;
 #ifdef PK_DECODE_NSTAGE
-  static constexpr int NSTAGE = PK_DECODE_NSTAGE;
+  static constexpr int NSTAGE16 = PK_DECODE_NSTAGE;
 #else
   static constexpr int RAW = PK_DECODE_INFLIGHT_BYTES / STAGE;
-  static constexpr int NSTAGE = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
+  static constexpr int NSTAGE16 = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
 #endif
+  // e4m3 stages hold half the bytes: more of them keep as much in flight
+  static constexpr int NSTAGE = FP8 ? PK_DECODE_FP8_NSTAGE : NSTAGE16;
 };
 
 // Programmatic stream serialisation: the kernel may be scheduled before its
@@ -445,12 +501,11 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int D, int BS>
-cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                            cudaStream_t stream) {
-  using T = DecodeTuning<D, BS>;
-  using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE>;
-  auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE>;
+template <int D, int BS, bool FP8>
+cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream) {
+  using T = DecodeTuning<D, BS, FP8>;
+  using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE, FP8>;
+  auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
   static bool attr_done = false;  // per process: the attribute belongs to the function
   if (!attr_done) {
     cudaError_t e =
@@ -459,8 +514,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap& kmap, const 
     attr_done = true;
   }
   dim3 grid(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts);
-  cudaError_t e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, kmap,
-                             vmap, a);
+  cudaError_t e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
   if (e != cudaSuccess) return e;
   if (a.num_parts > 1) {
     int w = a.num_parts / 8;
@@ -477,10 +531,11 @@ bool decode_supported(int D, int block_size) {
          (block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream) {
-#define PK_CASE(DD, BB) \
-  if (a.D == DD && a.block_size == BB) return launch_decode_t<DD, BB>(a, kmap, vmap, stream);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream) {
+#define PK_CASE(DD, BB)                                              \
+  if (a.D == DD && a.block_size == BB)                               \
+    return a.fp8 ? launch_decode_t<DD, BB, true>(a, maps, stream)    \
+                 : launch_decode_t<DD, BB, false>(a, maps, stream);
   PK_CASE(128, 16) PK_CASE(128, 32) PK_CASE(128, 8) PK_CASE(128, 4)
   PK_CASE(64, 16) PK_CASE(64, 32) PK_CASE(64, 8) PK_CASE(64, 4)
 #undef PK_CASE

@@ -38,6 +38,15 @@ struct DecodeArgs {
   const int32_t* group_offsets;  // [G+1] into group_seqs
   const int32_t* group_seqs;     // member sequence indices, the first one's table is read
   int num_groups, max_group_size, max_prefix_parts;
+  // FP8 (e4m3) pools: per-(token, head) fp32 scales laid out [num_blocks, H, bs].
+  bool fp8;
+  const float* k_scale;
+  const float* v_scale;
+};
+
+// The four tensor maps of a decode launch (scale maps used by FP8 pools only).
+struct DecodeMaps {
+  CUtensorMap k, v, ks, vs;
 };
 
 // Encodes the [num_blocks * block_size, H, D] view of a cache pool as a 3-D
@@ -50,11 +59,11 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, in
 // shared-memory swizzle (the inner box must then be 64 fp16 = 128 bytes).
 cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long long dims[3],
                         const unsigned long long strides[2], const unsigned box[3],
-                        bool swizzle128);
+                        bool swizzle128,
+                        CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 
 // Launch the partition kernel then the combine kernel on `stream`.
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream);
 bool decode_supported(int D, int block_size);
 bool prefix_supported(int D, int block_size, int max_group_size);
 
@@ -66,6 +75,11 @@ cudaError_t launch_prefix(const DecodeArgs& a, const CUtensorMap& kmap_sw,
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
                                   int H, int D, long long n_slots, __half* kc, __half* vc,
                                   int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_kv_cache_write_fp8(const __half* k, const __half* v, const int64_t* slots,
+                                      int T, int H, int D, int block_size, long long n_slots,
+                                      uint8_t* k8, uint8_t* v8, float* k_scale, float* v_scale,
+                                      int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_block_copy(__half* kc, __half* vc, const int64_t* pairs, int N,
                               long long block_elems, int num_blocks, int32_t* status,
