@@ -309,38 +309,70 @@ def cpu_baseline(batch, budget_s):
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
+def compact_sample(batch, n, heads=None):
+    """The first n sequences of the batch (and only the first `heads` heads)
+    on a pool holding only their blocks, tables and slots renumbered, so a
+    CPU step costs in proportion to the sample."""
+    bs = batch.block_size
+    hh = batch.H if heads is None else heads
+    ctx = batch.context_lens.cpu().numpy()[:n]
+    bt = batch.block_tables.cpu().numpy()[:n]
+    used = []
+    for b in range(n):
+        used.extend(int(x) for x in bt[b, :-(-int(ctx[b]) // bs)])
+    uniq = sorted(set(used))
+    remap = {old: new for new, old in enumerate(uniq)}
+    idx = torch.as_tensor(uniq, dtype=torch.int64)
+    kc = batch.k_cache.cpu()[idx][:, :, :hh].contiguous().numpy()
+    vc = batch.v_cache.cpu()[idx][:, :, :hh].contiguous().numpy()
+    bt2 = np.full_like(bt, -1)
+    for b in range(n):
+        nb = -(-int(ctx[b]) // bs)
+        bt2[b, :nb] = [remap[int(x)] for x in bt[b, :nb]]
+    slots = batch.slot_mapping.cpu().numpy()[:n]
+    slots2 = np.array([remap[int(s_) // bs] * bs + int(s_) % bs for s_ in slots], np.int64)
+    return (batch.q.cpu()[:n, :hh].contiguous().numpy(), kc, vc, bt2, ctx,
+            batch.k_new.cpu()[:n, :hh].contiguous().numpy(),
+            batch.v_new.cpu()[:n, :hh].contiguous().numpy(), slots2)
+
+
 def run_reference(args):
     import oracle
     batch = make_workload("cpu", seed=1)
     H, D, bs = batch.H, batch.D, batch.block_size
-    kc = batch.k_cache.numpy()
-    vc = batch.v_cache.numpy()
-    q, bt, ctx = batch.q.numpy(), batch.block_tables.numpy(), batch.context_lens.numpy()
-    kn, vn, sm = batch.k_new.numpy(), batch.v_new.numpy(), batch.slot_mapping.numpy()
+    ctx_all = batch.context_lens.numpy()
     budget = args.reference_budget_s / max(args.steps + args.warmup, 1)
+    # calibrate: the oracle's cost per attended (key, head) on one sequence, one head
+    one = compact_sample(batch, 1, heads=1)
     t0 = time.perf_counter()
-    oracle.decode(q[:1], kc, vc, bt[:1], ctx[:1], batch.scale)
-    per_token = (time.perf_counter() - t0) / int(ctx[0])
-    n = 1
-    while n < len(ctx) and per_token * ctx[:n + 1].sum() < budget:
-        n += 1
+    kc2, vc2 = oracle.kv_cache_write(one[5], one[6], one[7], one[1], one[2])
+    oracle.decode(one[0], kc2, vc2, one[3], one[4], batch.scale)
+    per_key_head = (time.perf_counter() - t0) / int(ctx_all[0])
+    n, heads = 1, H
+    if per_key_head * ctx_all[0] * H > budget:  # less than one whole sequence: fewer heads
+        heads = int(max(1, min(H, budget // (per_key_head * ctx_all[0]))))
+    else:
+        while n < len(ctx_all) and per_key_head * H * ctx_all[:n + 1].sum() < budget:
+            n += 1
+    q, kc, vc, bt, ctx, kn, vn, sm = compact_sample(batch, n, heads)
 
-    def one():
+    def one_step():
         kc2, vc2 = oracle.kv_cache_write(kn, vn, sm, kc, vc)
-        oracle.decode(q[:n], kc2, vc2, bt[:n], ctx[:n], batch.scale)
+        oracle.decode(q, kc2, vc2, bt, ctx, batch.scale)
 
     for _ in range(args.warmup):
-        one()
+        one_step()
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        one()
+        one_step()
         ts.append(time.perf_counter() - t0)
-    byts = decode_bytes(ctx[:n], n, H, D, bs) + write_bytes(len(sm), H, D)
+    byts = decode_bytes(ctx, n, heads, D, bs) + write_bytes(n, heads, D)
     secs = sum(ts)
     value = byts * args.steps / secs / 1e9
-    sample = (f"cache write of {len(sm)} tokens + decode of the first {n} of {len(ctx)} "
-              f"sequences ({int(ctx[:n].sum())} keys x {H} heads) per step, fp64, one thread")
+    sample = (f"cache write of {n} new token(s) + decode of the first {n} of {len(ctx_all)} "
+              f"sequences, {heads} of {H} heads ({int(ctx.sum())} keys) per step, on a pool "
+              "of only their blocks; fp64, one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
