@@ -14,25 +14,26 @@
 //   warp 8      TMA producer: Q (4 boxes of 128 rows x 64 dims, 128-byte
 //               swizzle), then per key tile one box per (block, 64-dim half)
 //               for K and for V, gathered through the block table, into a
-//               5-stage ring shared by both Q tiles (two key tiles ahead);
-//   warp 9      MMA issuer (one thread) and tensor-memory owner, in ping-pong
-//               order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while one tile's
-//               softmax runs the tensor core works on the other tile.
-// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512);
-// P_X (fp16 pairs packed per 32-bit column) overwrites the first 64 columns
-// of S_X once the softmax holds S_X in registers, and the P V MMA reads it
-// from tensor memory.  Because tcgen05 operations of one thread complete in
-// issue order, "S_X(j+1) done" implies "P_X(j) V_j done": the softmax may
-// then rescale O_X without any further barrier.
-// Softmax per tile: two tensor-memory round trips over the S row, one for
-// the row max (keys past the row's position skipped on diagonal tiles), one
-// for p = 2^(s*scale*log2e - m) (one FMA and one ex2 per element); between
-// them the output accumulator is rescaled, only when the row max grew by more
-// than 2^8 (P then stays <= 256, exact in fp16 range).  The row is summed and
-// P (fp16) stored to tensor memory.
+//               3-slot ring in first-use order K_0, K_1, V_0, K_2, V_1, ...;
+//   warp 9      S issuer (one thread) and tensor-memory owner;
+//   warp 10     P V issuer (one thread).
+// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Softmax of tile X, key tile j: wait for S_X(j), load the whole row into
+// registers and release S_X at once, so the tensor core computes S_X(j+1)
+// while this softmax still works on j.  Row max (keys past the row's position
+// skipped on diagonal tiles); p = 2^(s*scale*log2e - m) (one FMA, one ex2)
+// packed to fp16 in registers with the row sum; then wait for P_X(j-1) V_{j-1}
+// (so O_X is stable and the P_X tile free), rescale O_X only when the row max
+// grew by more than 2^8 (P then stays <= 256, exact in fp16 range), store P_X
+// to shared memory.
+// S_X(j+1) is issued once the softmax of X released S_X(j) and K_{j+1}
+// landed; O_X += P_X(j) V_j once P_X(j) is stored and V_j landed.  The two
+// kinds come from two threads, so a P V product that gates a softmax never
+// queues behind S products at the issuing end.
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle):
-//   Q, K_j      : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
-//                 the two 64-element halves 16 KB apart;
+//   Q, P, K_j   : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
+//                 the two 64-element halves 16 KB apart; the 16-byte chunk c
+//                 of row r sits at chunk position c ^ (r mod 8);
 //   V_j         : MN-major (dims contiguous): 8-key atoms 1024 B apart along
 //                 K, the two 64-dim halves 16 KB apart along N.
 #include "pk_common.cuh"
@@ -49,35 +50,43 @@ constexpr int kTileN = 128;                  // keys per tile
 constexpr int kD = 128;                      // head dim
 constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
 constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
-constexpr int kStages = 5;                   // K/V ring (K and V tiles alternate)
-constexpr int kThreads = 320;                // 8 softmax warps + producer + MMA
+constexpr int kStages = 3;                   // K/V ring, tiles in first-use order
+constexpr int kThreads = 352;                // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpMma = 9;                  // S = Q K^T issuer, tensor-memory owner
+constexpr int kWarpPv = 10;                  // O += P V issuer
 constexpr int kTblWindow = 256;              // block-table entries staged in smem
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 
 constexpr int kOffQ = 0;                                // Q_A, Q_B
-constexpr int kOffKV = kOffQ + 2 * kTileBytes;
+constexpr int kOffP = kOffQ + 2 * kTileBytes;           // P_A, P_B
+constexpr int kOffKV = kOffP + 2 * kTileBytes;
 constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
 constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
 constexpr int kOffTbl = (kOffTmemHolder + 4 + 15) / 16 * 16;
 constexpr int kSmemBytes = kOffTbl + kTblWindow * 4 + 1024;  // + alignment slack
 
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kIdescS = tc::idesc_f16_f32(kTileM, kTileN, false, false);
 constexpr uint32_t kIdescO = tc::idesc_f16_f32(kTileM, kD, false, true);
+constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
-  // K step kk (16 elements = 32 B) inside the 64-element half kk / 4.
-  return tc::smem_desc(tile_addr + (kk >> 2) * kSlabBytes + (kk & 3) * 32, 16, 1024,
-                       tc::kSwizzle128B);
+// Descriptor address offset of K step kk (16 elements = 32 B) of a K-major
+// tile: inside the 64-element half kk / 4.
+__device__ __forceinline__ constexpr uint32_t kmajor_off(int kk) {
+  return (uint32_t)((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
+}
+// ... of an MN-major V tile: keys 16*kk .. 16*kk+15 are two 8-key atoms
+// starting 2048 B * kk into the tile.
+__device__ __forceinline__ constexpr uint32_t vmn_off(int kk) {
+  return (uint32_t)(kk * 2048) >> 4;
 }
 
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile_addr, int kk) {
-  // keys 16*kk .. 16*kk+15: two 8-key atoms starting 2048 B * kk into the tile.
-  return tc::smem_desc(tile_addr + kk * 2048, kSlabBytes, 1024, tc::kSwizzle128B);
-}
+// Ring load index of K_t and V_t (loads go K_0, then K_{t+1}, V_t per t).
+__device__ __forceinline__ int load_k(int t) { return t == 0 ? 0 : 2 * t - 1; }
+__device__ __forceinline__ int load_v(int t, int n_kv) { return t + 1 < n_kv ? 2 * t + 2 : 2 * t + 1; }
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -90,15 +99,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
   uint8_t* sQ = smem + kOffQ;
+  uint8_t* sP = smem + kOffP;
   uint8_t* sKV = smem + kOffKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;  // [2]: per Q tile
-  uint64_t* p_full = s_full + 2;          // [2]
-  uint64_t* o_done = p_full + 2;          // [2]
-  uint64_t* drain = o_done + 2;
+  uint64_t* s_full = kv_empty + kStages;  // [2] per Q tile: S_X(j) computed
+  uint64_t* s_free = s_full + 2;          // [2]: softmax holds S_X(j) in registers
+  uint64_t* p_full = s_free + 2;          // [2]: P_X(j) stored
+  uint64_t* pv_done = p_full + 2;         // [2]: O_X += P_X(j) V_j completed
+  uint64_t* drain = pv_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
   int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
 
@@ -119,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   // Per Q tile (A = 0, B = 1): rows, sequence position of row 0, key tiles.
+  // ntile_a <= ntile_b whenever tile B has rows.
   const int rows_a = min(kTileM, a.Lq - q0);
   const int rows_b = max(0, min(kTileM, a.Lq - (q0 + kTileM)));
   const int pos0_a = n - a.Lq + q0;
@@ -136,10 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
       mbar_init(&p_full[i], 128);
-      mbar_init(&o_done[i], 1);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -157,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     int win = -kTblWindow;
     if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
       const int bh = b * a.H + h;
       mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
 #pragma unroll
@@ -165,10 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ + x * kTileBytes + kSlabBytes, &qmap, 64, q0 + x * kTileM, bh, q_full);
       }
     }
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int lb0 = j * BPT;
-      if (lb0 + BPT > win + kTblWindow) {
-        win = lb0;
+    // Key tile t (K when v == 0, else V) into ring slot u % kStages.
+    auto load_tile = [&](int t, int v, int u) {
+      const int lb0 = t * BPT;
+      if (lb0 < win || lb0 + BPT > win + kTblWindow) {
+        // K_t is requested before V_{t-1}: start the window one tile early.
+        win = (v == 0 && t > 0) ? lb0 - BPT : lb0;
         __syncwarp();
         for (int i = lane; i < kTblWindow; i += 32) {
           const int lb = win + i;
@@ -184,75 +201,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      for (int half = 0; half < 2 && ok; ++half) {  // K tile, then V tile
-        const int u = 2 * j + half;
-        const int st = u % kStages;
-        if (lane == 0) {
-          ok = mbar_wait(&kv_empty[st], ((u / kStages) & 1) ^ 1);
-          if (ok) {
-            uint8_t* dst = sKV + st * kTileBytes;
-            const CUtensorMap* map = half ? &vmap : &kmap;
-            mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
-#pragma unroll
-            for (int i = 0; i < BPT; ++i) {
-              const int row = tbl_s[lb0 - win + i] * BS;
-              tma_load_3d(dst + i * BS * 128, map, 0, h, row, &kv_full[st]);
-              tma_load_3d(dst + kSlabBytes + i * BS * 128, map, 64, h, row, &kv_full[st]);
-            }
-            ++issued;
-          }
-        }
-        ok = __shfl_sync(kFull, ok, 0);
+      const int st = u % kStages;
+      if (lane == 0) {
+        ok = mbar_wait(&kv_empty[st], ((u / kStages) & 1) ^ 1);
+        if (ok) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
       }
+      ok = __shfl_sync(kFull, ok, 0);
+      // One box per lane (block lane / 2, 64-dim half lane % 2): a single
+      // thread would spend about 100 cycles per box issuing them in turn.
+      if (ok && lane < 2 * BPT) {
+        const int i = lane >> 1, hf = lane & 1;
+        uint8_t* dst = sKV + st * kTileBytes + hf * kSlabBytes + i * BS * 128;
+        tma_load_3d(dst, v ? &vmap : &kmap, hf * 64, h, tbl_s[lb0 - win + i] * BS, &kv_full[st]);
+      }
+      if (ok && lane == 0) ++issued;
+    };
+    int u = 0;
+    if (n_kv > 0) load_tile(0, 0, u++);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      if (j + 1 < n_kv) load_tile(j + 1, 0, u++);
+      if (ok) load_tile(j, 1, u++);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads: S_X(t) = Q_X K_t^T once the softmax of X released S_X(t-1)
+    // and K_t landed; O_X (+)= P_X(t) V_t once P_X(t) is stored and V_t
+    // landed.  Each thread's commits track its own MMAs, and K is read only
+    // by the first, V and O only by the second.
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t kv_addr = smem_u32(sKV);
-      // S_X(j) = Q_X K_j^T; releases K_j when X is its last user.
-      auto issue_s = [&](int x, int j, bool release) -> bool {
-        const int u = 2 * j;
-        const int st = u % kStages;
-        if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t qa = q_addr + x * kTileBytes;
-        const uint32_t kb = kv_addr + st * kTileBytes;
+      const int nt[2] = {ntile_a, ntile_b};
+      auto landed = [&](int u) { return mbar_wait(&kv_full[u % kStages], (u / kStages) & 1); };
+      if (warp == kWarpMma) {
+        // Base descriptors; each MMA adds a compile-time offset (a slot, a
+        // tile or a K step never carries out of the 14-bit address field).
+        const uint64_t dq = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128B);
+        const uint64_t dk = tc::smem_desc(smem_u32(sKV), 16, 1024, tc::kSwizzle128B);
+        ok = mbar_wait(q_full, 0);
+        for (int t = 0; t < n_kv && ok; ++t) {
+          const int u = load_k(t);
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (t >= nt[x]) continue;
+            if (t > 0 && !(ok = mbar_wait(&s_free[x], (t - 1) & 1))) break;
+            if (!(ok = landed(u))) break;
+            tc::fence_after_sync();
+            const uint64_t da = dq + x * kTileDesc;
+            const uint64_t db = dk + (u % kStages) * kTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          tc::mma_f16(tmem + x * kTileN, kmajor_desc(qa, kk), kmajor_desc(kb, kk), kIdescS,
-                      kk > 0);
-        tc::commit(&s_full[x]);
-        if (release) tc::commit(&kv_empty[st]);
-        return true;
-      };
-      // O_X += P_X V_j once the softmax of X has written P_X for tile j.
-      auto issue_pv = [&](int x, int j, int ntile) -> bool {
-        if (!mbar_wait(&p_full[x], j & 1)) return false;
-        const int u = 2 * j + 1;
-        const int st = u % kStages;
-        if (!mbar_wait(&kv_full[st], (u / kStages) & 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t vb = kv_addr + st * kTileBytes;
+            for (int kk = 0; kk < kD / 16; ++kk)
+              tc::mma_f16(tmem + x * kTileN, da + kmajor_off(kk), db + kmajor_off(kk), kIdescS,
+                          kk > 0);
+            tc::commit(&s_full[x]);
+          }
+          if (ok) tc::commit(&kv_empty[u % kStages]);  // K_t has no further reader
+        }
+      } else {
+        const uint64_t dp = tc::smem_desc(smem_u32(sP), 16, 1024, tc::kSwizzle128B);
+        const uint64_t dv = tc::smem_desc(smem_u32(sKV), kSlabBytes, 1024, tc::kSwizzle128B);
+        for (int t = 0; t < n_kv && ok; ++t) {
+          const int u = load_v(t, n_kv);
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (t >= nt[x]) continue;
+            if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
+            if (!(ok = landed(u))) break;
+            tc::fence_after_sync();
+            const uint64_t da = dp + x * kTileDesc;
+            const uint64_t db = dv + (u % kStages) * kTileDesc;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // P columns: 16 keys = 8 packed columns
-          tc::mma_f16_ts(tmem + kColO + x * kD, tmem + x * kTileN + kk * 8, vmn_desc(vb, kk),
-                         kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (j == ntile - 1) tc::commit(&o_done[x]);
-        return true;
-      };
-      ok = mbar_wait(q_full, 0);
-      if (ok) {
-        tc::fence_after_sync();
-        ok = issue_s(0, 0, ntile_b == 0);
-        if (ok && ntile_b > 0) ok = issue_s(1, 0, true);
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j < ntile_a && !(ok = issue_pv(0, j, ntile_a))) break;
-        if (j + 1 < ntile_a && !(ok = issue_s(0, j + 1, j + 1 >= ntile_b))) break;
-        if (j < ntile_b && !(ok = issue_pv(1, j, ntile_b))) break;
-        tc::commit(&kv_empty[(2 * j + 1) % kStages]);  // V_j has no further reader
-        if (j + 1 < ntile_b && !(ok = issue_s(1, j + 1, true))) break;
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              tc::mma_f16(tmem + kColO + x * kD, da + kmajor_off(kk), db + vmn_off(kk), kIdescO,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+            tc::commit(&pv_done[x]);
+          }
+          if (ok) tc::commit(&kv_empty[u % kStages]);  // V_t has no further reader
+        }
       }
     }
     ok = __shfl_sync(kFull, ok, 0);
@@ -269,35 +290,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntile = x ? ntile_b : ntile_a;
     const int rows = x ? rows_b : rows_a;
     const float sl2 = a.scale_log2;
+    uint8_t* prow = sP + x * kTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < ntile && ok; ++j) {
       if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
       const int kbase = j * kTileN;
       const bool diag = kbase + kTileN - 1 > pos0;  // some key here is past some row
-      // Row max: the whole S row in one tensor-memory round trip (4 loads, one
-      // wait); keys past this row's position are skipped on diagonal tiles.
-      float mx[8];
-      {
-        uint32_t r[4][32];
+      // The whole S row in registers; S_X is then free for S_X(j+1).
+      uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld_32x32(t_s + c * 32, r[c]);
-        tc::wait_ld();
+      for (int c = 0; c < 4; ++c) tc::ld_32x32(t_s + c * 32, r[c]);
+      tc::wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(&s_free[x]);
+      if (diag) {  // keys past this row's position: -inf
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-        if (diag) {
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (kbase + c * 32 + i <= pos) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
-        }
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i > pos) r[c][i] = __float_as_uint(-INFINITY);
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       const float m_new = fmaxf(m, mt);
@@ -308,8 +328,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
         l *= alpha;
       }
+      // P = 2^(s * scale * log2e - m) packed to fp16 pairs in place (the
+      // first 16 words of each 32-key chunk), row sum.  A masked key has
+      // s = -inf, so p = 0.
+      const float neg_m = -m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), sl2, neg_m));
+          rs[e & 3] += p0 + p1;
+          __half2 hp = __floats2half2_rn(p0, p1);
+          r[c][e] = *reinterpret_cast<uint32_t*>(&hp);
+        }
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      // P_X(j-1) V_{j-1} done: the P_X tile is free, O_X is stable.
+      if (j > 0) {
+        if (!(ok = __all_sync(kFull, mbar_wait(&pv_done[x], (j - 1) & 1)))) break;
+        tc::fence_after_sync();
+      }
       if (j > 0 && __any_sync(kFull, resc)) {
-        // S_X(j) has completed, hence so has P_X(j-1) V_{j-1}: rescale O_X.
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -321,38 +361,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::wait_st();
       }
-      // P = 2^(s * scale * log2e - m) in fp16, row sum: S reloaded 32 columns
-      // at a time, P stored over the first 64 columns of S_X.
-      const float neg_m = -m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // Store P: 32 keys = four 16-byte chunks, swizzled like the TMA tiles.
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 packed columns per store
-        uint32_t r[32];
-        tc::ld_32x32(t_s + c * 32, r);
-        tc::wait_ld();
-        uint32_t pk[16];
+      for (int c = 0; c < 4; ++c) {
+        uint8_t* slab = prow + (c >> 1) * kSlabBytes;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i0 = 2 * e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[i0]), sl2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[i0 + 1]), sl2, neg_m));
-          if (diag) {
-            if (kbase + c * 32 + i0 > pos) p0 = 0.f;
-            if (kbase + c * 32 + i0 + 1 > pos) p1 = 0.f;
-          }
-          rs[e & 3] += p0 + p1;
-          __half2 hp = __floats2half2_rn(p0, p1);
-          pk[e] = *reinterpret_cast<uint32_t*>(&hp);
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = (((c & 1) << 2) + q) ^ (row & 7);
+          *reinterpret_cast<uint4*>(slab + chunk * 16) =
+              make_uint4(r[c][4 * q], r[c][4 * q + 1], r[c][4 * q + 2], r[c][4 * q + 3]);
         }
-        // P columns [16c, 16c+16) lie below S columns [32c, ...) not yet read.
-        tc::st_32x16(t_s + c * 16, pk);
       }
-      tc::wait_st();
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
       tc::fence_before_sync();
       mbar_arrive(&p_full[x]);
     }
-    if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&o_done[x], 0));
+    if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&pv_done[x], (ntile - 1) & 1));
     if (ok && ntile > 0) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
@@ -390,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = max(0, issued - kStages); u < issued; ++u)
         mbar_wait(&kv_full[u % kStages], (u / kStages) & 1);
     }
-    if (warp == kWarpMma && lane == 0) {
+    if ((warp == kWarpMma || warp == kWarpPv) && lane == 0) {
       tc::commit(drain);
       mbar_wait(drain, 0);
     }
