@@ -69,31 +69,60 @@ struct LaneVec<2> {
   }
 };
 
-// EPL e4m3 codes of one lane (FP8 pools), decoded exactly to float.
+// Sum of a.lo*b.lo + a.hi*b.hi + c for fp16 pairs a, b: products exact in fp32,
+// each addition rounded once, in this order (the same value as converting a
+// and b to float and chaining fmaf).
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.f16 t, a0, b0, %3;\n\tfma.rn.f32.f16 %0, a1, b1, t;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Lane partial of q . k for EPL e4m3 codes of k (fp16 query pairs qh).
 template <int EPL>
-struct LaneVec8;
-template <>
-struct LaneVec8<4> {
-  uint32_t raw;
-  __device__ __forceinline__ void load(const uint8_t* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
-  __device__ __forceinline__ void to_float(float* f) const {
+__device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) {
+  if constexpr (EPL == 4) {
+    const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  }
-};
-template <>
-struct LaneVec8<2> {
-  uint16_t raw;
-  __device__ __forceinline__ void load(const uint8_t* p) { raw = *reinterpret_cast<const uint16_t*>(p); }
-  __device__ __forceinline__ void to_float(float* f) const {
+    const float t = fma2_f16_f32(qh[0], *reinterpret_cast<const uint32_t*>(&lo), 0.f);
+    return fma2_f16_f32(qh[1], *reinterpret_cast<const uint32_t*>(&hi), t);
+  } else {
+    const uint16_t raw = *reinterpret_cast<const uint16_t*>(p);
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)raw, __NV_E4M3);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-    f[0] = a.x; f[1] = a.y;
+    return fma2_f16_f32(qh[0], *reinterpret_cast<const uint32_t*>(&lo), 0.f);
   }
-};
+}
+
+// o[e] += w * v[e] for EPL e4m3 codes v (exact in fp16), products exact in
+// fp32, one rounding per addition.
+template <int EPL>
+__device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint8_t* p) {
+  const uint16_t wb = __half_as_ushort(w);
+  if constexpr (EPL == 4) {
+    const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
+    asm("{\n\t.reg .f16 w, b0, b1, b2, b3;\n\tmov.b16 w, %4;\n\t"
+        "mov.b32 {b0, b1}, %5;\n\tmov.b32 {b2, b3}, %6;\n\t"
+        "fma.rn.f32.f16 %0, w, b0, %0;\n\tfma.rn.f32.f16 %1, w, b1, %1;\n\t"
+        "fma.rn.f32.f16 %2, w, b2, %2;\n\tfma.rn.f32.f16 %3, w, b3, %3;\n\t}"
+        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
+        : "h"(wb), "r"(*reinterpret_cast<const uint32_t*>(&lo)),
+          "r"(*reinterpret_cast<const uint32_t*>(&hi)));
+  } else {
+    const uint16_t raw = *reinterpret_cast<const uint16_t*>(p);
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)raw, __NV_E4M3);
+    asm("{\n\t.reg .f16 w, b0, b1;\n\tmov.b16 w, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, w, b0, %0;\n\tfma.rn.f32.f16 %1, w, b1, %1;\n\t}"
+        : "+f"(o[0]), "+f"(o[1])
+        : "h"(wb), "r"(*reinterpret_cast<const uint32_t*>(&lo)));
+  }
+}
 
 template <int EPL>
 __device__ __forceinline__ void store_half_row(__half* dst, const float* v) {
@@ -193,12 +222,16 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
 
-  // Query slice of this lane.
+  // Query slice of this lane (and, for e4m3 pools, its fp16 pairs).
   float qf[EPL];
+  uint32_t qh[EPL / 2];
   {
     LaneVec<EPL> qv;
     qv.load(a.q + row_bh * D + lane * EPL);
     qv.to_float(qf);
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e)
+      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + lane * EPL)[e];
   }
 
   if (lane == 0) {
@@ -272,20 +305,18 @@ __global__ void __launch_bounds__(WARPS * 32)
     float part_dot[TB];
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
-      float kf[EPL];
       if constexpr (FP8) {
-        LaneVec8<EPL> kv;
-        kv.load(kst + t * D + lane * EPL);
-        kv.to_float(kf);
+        part_dot[t] = dot_e4m3<EPL>(qh, kst + t * D + lane * EPL);
       } else {
+        float kf[EPL];
         LaneVec<EPL> kv;
         kv.load(ks + t * D + lane * EPL);
         kv.to_float(kf);
-      }
-      float acc = 0.f;
+        float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
-      part_dot[t] = acc;
+        for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+        part_dot[t] = acc;
+      }
     }
     // Transposing butterfly: after round r, lanes keep half of the tokens.
 #pragma unroll
@@ -318,23 +349,24 @@ __global__ void __launch_bounds__(WARPS * 32)
     l = l * alpha + psum;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
+    // e4m3 pools: the weight p * v_scale goes to fp16 (relative error 2^-11)
+    // times 2^8, which keeps it in the normal fp16 range; o carries the 2^8
+    // until the partition writes it.
+    const float pr_v = FP8 ? pr * 256.f : pr;
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
-      float pt = __shfl_sync(kFull, pr, t * LPT);
+      const float pt = __shfl_sync(kFull, pr_v, t * LPT);
       if (t < valid) {
-        float vf[EPL];
         if constexpr (FP8) {
-          pt *= vscl[t];  // fold the V row's scale into its weight
-          LaneVec8<EPL> vv;
-          vv.load(kst + Cfg::TILE_BYTES + t * D + lane * EPL);
-          vv.to_float(vf);
+          axpy_e4m3<EPL>(o, __float2half_rn(pt * vscl[t]), kst + Cfg::TILE_BYTES + t * D + lane * EPL);
         } else {
+          float vf[EPL];
           LaneVec<EPL> vv;
           vv.load(vs + t * D + lane * EPL);
           vv.to_float(vf);
-        }
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
+          for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
+        }
       }
     }
     m = m_new;
@@ -357,6 +389,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     return;
   }
 
+  if constexpr (FP8) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] *= 1.f / 256.f;  // exact
+  }
   const int n_parts = (ctx + a.part_tokens - 1) / a.part_tokens;
   if (n_parts == 1) {
     const float inv = 1.f / l;
