@@ -281,18 +281,15 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
     a.num_groups = groups->num_groups;
     a.max_group_size = groups->max_group_size;
     a.max_prefix_parts = prefix_parts;
-    // 64-dim halves in 128-byte swizzle for the prefix kernel's ldmatrix reads
-    CUtensorMap ksw, vsw;
+    // 64-dim halves in 128-byte swizzle for the shared-prefix ldmatrix reads
     const unsigned long long dims[3] = {(unsigned long long)D, (unsigned long long)H,
                                         (unsigned long long)rows};
     const unsigned long long strides[2] = {(unsigned long long)D * 2,
                                            (unsigned long long)H * D * 2};
     const unsigned box[3] = {64, 1, 16};
-    if (pk::make_map_3d(&ksw, k_cache, dims, strides, box, true) != cudaSuccess ||
-        pk::make_map_3d(&vsw, v_cache, dims, strides, box, true) != cudaSuccess)
+    if (pk::make_map_3d(&maps.ksw, k_cache, dims, strides, box, true) != cudaSuccess ||
+        pk::make_map_3d(&maps.vsw, v_cache, dims, strides, box, true) != cudaSuccess)
       return PA_ERR_INVALID;
-    e = pk::launch_prefix(a, ksw, vsw, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
   }
   e = pk::launch_decode(a, maps, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);

@@ -40,6 +40,7 @@
 
 #include "pk_common.cuh"
 #include "pk_internal.h"
+#include "pk_prefix.cuh"
 
 namespace pk {
 
@@ -167,7 +168,9 @@ struct PartitionCfg {
   static constexpr int SMEM_BYTES = WARPS * NSTAGE * STAGE_BYTES + WARPS * NSTAGE * 8;
 };
 
-template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
+// GRP: grouped call (a.seq_group set) that also runs shared-prefix partitions;
+// a separate instantiation so plain decode keeps its small register budget.
+template <int D, int BS, int WARPS, int NSTAGE, bool FP8, bool GRP = false>
 __global__ void __launch_bounds__(WARPS * 32)
     partition_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
   using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE, FP8>;
@@ -193,11 +196,21 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
   const int tok0 = part * a.part_tokens;
   const size_t row_bh = (size_t)b * a.H + h;
-  if (a.seq_group != nullptr) {  // partitions inside the group's shared prefix: prefix kernel
+  if (a.seq_group != nullptr) {  // partitions inside the group's shared prefix
     const int g = a.seq_group[b];
     if (g >= 0 && g < a.num_groups) {
       const int shared = min(a.group_prefix_len[g], ctx) / a.part_tokens * a.part_tokens;
-      if (tok0 + a.part_tokens <= shared) return;
+      if (tok0 + a.part_tokens <= shared) {
+        if constexpr (GRP && !FP8 && BS % 16 == 0) {
+          // The group's first member computes this partition for every member.
+          if (a.group_seqs[a.group_offsets[g]] == b) {
+            const uint32_t sa = smem_u32(smem);
+            pfx::prefix_partition<D, BS, WARPS>(maps.ksw, maps.vsw, a, g, part,
+                                                smem + ((1024u - (sa & 1023u)) & 1023u));
+          }
+        }
+        return;
+      }
     }
   }
   if (tok0 >= ctx) {
@@ -541,16 +554,32 @@ template <int D, int BS, bool FP8>
 cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream) {
   using T = DecodeTuning<D, BS, FP8>;
   using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE, FP8>;
-  auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
-  static bool attr_done = false;  // per process: the attribute belongs to the function
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
   dim3 grid(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts);
-  cudaError_t e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
+  cudaError_t e;
+  bool grouped = false;
+  if constexpr (!FP8 && BS % 16 == 0) grouped = a.seq_group != nullptr;
+  if (!grouped) {
+    auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
+    static bool attr_done = false;  // per process: the attribute belongs to the function
+    if (!attr_done) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_done = true;
+    }
+    e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
+  } else if constexpr (!FP8 && BS % 16 == 0) {
+    // The grouped grid also runs the shared-prefix partitions.
+    constexpr int kPfxSmem = pfx::PrefixCfg<D, T::WARPS>::SMEM;
+    constexpr int kSmem = Cfg::SMEM_BYTES > kPfxSmem ? Cfg::SMEM_BYTES : kPfxSmem;
+    auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8, true>;
+    static bool attr_done = false;
+    if (!attr_done) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      attr_done = true;
+    }
+    e = launch_pdl(kern, grid, dim3(T::WARPS * 32), kSmem, stream, maps, a);
+  }
   if (e != cudaSuccess) return e;
   if (a.num_parts > 1) {
     int w = a.num_parts / 8;
@@ -561,6 +590,11 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
 }
 
 }  // namespace
+
+bool prefix_supported(int D, int block_size, int max_group_size) {
+  return (D == 64 || D == 128) && (block_size == 16 || block_size == 32) &&
+         max_group_size >= 1 && max_group_size <= pfx::kMaxMembers;
+}
 
 bool decode_supported(int D, int block_size) {
   return (D == 64 || D == 128) &&

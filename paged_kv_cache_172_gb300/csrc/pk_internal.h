@@ -47,6 +47,7 @@ struct DecodeArgs {
 // The four tensor maps of a decode launch (scale maps used by FP8 pools only).
 struct DecodeMaps {
   CUtensorMap k, v, ks, vs;
+  CUtensorMap ksw, vsw;  // 64-dim halves, 128-byte swizzle (grouped calls' shared prefix)
 };
 
 // Encodes the [num_blocks * block_size, H, D] view of a cache pool as a 3-D
@@ -62,15 +63,12 @@ cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long 
                         bool swizzle128,
                         CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 
-// Launch the partition kernel then the combine kernel on `stream`.
+// Launch the partition kernel then the combine kernel on `stream`.  When
+// a.seq_group is set, the partition grid also computes the groups' shared-
+// prefix partitions (multi-query, from maps.ksw / maps.vsw).
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream);
 bool decode_supported(int D, int block_size);
 bool prefix_supported(int D, int block_size, int max_group_size);
-
-// Multi-query partials of the shared-prefix partitions (launched before
-// launch_decode when a.seq_group is set).
-cudaError_t launch_prefix(const DecodeArgs& a, const CUtensorMap& kmap_sw,
-                          const CUtensorMap& vmap_sw, cudaStream_t stream);
 
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
                                   int H, int D, long long n_slots, __half* kc, __half* vc,

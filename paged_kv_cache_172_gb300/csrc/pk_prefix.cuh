@@ -1,4 +1,5 @@
-// decode_prefix.cu -- shared-prefix partitions of paged decode.
+// pk_prefix.cuh -- shared-prefix partitions of paged decode (device code included
+// by decode.cu: the partition kernel runs them in place of the partitions it skips).
 //
 // Sequences that share a prompt point at the same physical blocks (study
 // notes "DataWhale组队学习笔记--llm-algo-leetcode(五)", "4. PagedAttention 带来的
@@ -8,8 +9,11 @@
 // per group: a warp streams the shared blocks of one (group, head, partition)
 // and attends with every member's query at once, writing each member's
 // partition partial (max, normaliser, unnormalised output) to the decode
-// workspace; the ordinary partition kernel skips those partitions and the
-// combine kernel merges all partials of a sequence by log-sum-exp as usual.
+// workspace.  In the partition kernel's grid, the CTA of the group's first
+// member for such a partition does this work for the whole group and the
+// other members' CTAs return; the combine kernel merges all partials of a
+// sequence by log-sum-exp as usual.  One launch, so the group-wide
+// partitions overlap the members' private partitions.
 //
 // With up to 16 member queries the per-block work is a small dense product
 // (16 x 16 scores over D dims, then 16 x D outputs over 16 keys), done with
@@ -18,26 +22,26 @@
 // stages arrive by TMA in 128-byte-swizzled 64-dim halves (conflict-free
 // ldmatrix), and the score fragments become the P fragments of the second
 // product in registers.
+#pragma once
 #include "pk_common.cuh"
 #include "pk_internal.h"
 
 namespace pk {
+namespace pfx {
 
-namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kPfxFull = 0xffffffffu;
 constexpr int kMaxMembers = 16;  // rows of one m16n8k16 tile
 constexpr int kTB = 16;          // tokens per pipeline stage
-constexpr int kWarps = 4;        // heads per CTA
 constexpr int kStages = 2;
 
-template <int D>
+template <int D, int WARPS>
 struct PrefixCfg {
   static constexpr int SLABS = D / 64;             // 64-dim halves, 128-byte rows
   static constexpr int SLAB_BYTES = kTB * 128;     // 16 rows x 128 B
   static constexpr int TILE = SLABS * SLAB_BYTES;  // K (or V) of one stage
   static constexpr int STAGE = 2 * TILE;
-  static constexpr int SMEM = kWarps * kStages * STAGE + kWarps * kStages * 8 + 1024;
+  // per-warp stages, barriers, and slack to align the base to 1024 B
+  static constexpr int SMEM = WARPS * kStages * STAGE + WARPS * kStages * 8 + 1024;
   static constexpr int KSTEPS = D / 16;  // k-steps of the score product
   static constexpr int NT_O = D / 8;     // n-tiles of the output product
 };
@@ -78,29 +82,24 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ int seq_ctx(const DecodeArgs& a, int b) {
+__device__ __forceinline__ int seq_ctx(const DecodeArgs& a, int b) {  // clamped, silent
   int ctx = a.context_lens[b];
   const int cap = min(a.max_context_len, a.max_blocks * a.block_size);
   return ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
 }
 
-// Grid (G, ceil(H / kWarps), max shared partitions); warp = one head.
-template <int D, int BS>
-__global__ void __launch_bounds__(kWarps * 32)
-    prefix_kernel(const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using Cfg = PrefixCfg<D>;
+// One (group, head group, shared partition) unit: warp w of the CTA takes
+// head blockIdx.y * WARPS + w; smem is 1024-byte aligned, PrefixCfg::SMEM - 1024
+// bytes long.
+template <int D, int BS, int WARPS>
+__device__ __forceinline__ void prefix_partition(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                                 const DecodeArgs& a, int grp, int part,
+                                                 uint8_t* smem) {
+  using Cfg = PrefixCfg<D, WARPS>;
   constexpr int SUB = BS / kTB;
   static_assert(BS % kTB == 0, "block size must be a multiple of 16");
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = blockIdx.x;
-  const int h = blockIdx.y * kWarps + warp;
-  const int part = blockIdx.z;
-  pdl_wait();
+  const int h = blockIdx.y * WARPS + warp;
   if (h >= a.H) return;
   const int m0 = a.group_offsets[grp];
   const int mcount = a.group_offsets[grp + 1] - m0;
@@ -121,7 +120,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int nunit = a.part_tokens / kTB;
 
   uint8_t* wbase = smem + warp * kStages * Cfg::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * Cfg::STAGE) +
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WARPS * kStages * Cfg::STAGE) +
                    warp * kStages;
 
   // Shared block ids from the first member's table, one per lane.
@@ -166,7 +165,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncwarp();
   auto issue = [&](int u, int s) {
-    const int pb = __shfl_sync(kFull, phys, u / SUB);
+    const int pb = __shfl_sync(kPfxFull, phys, u / SUB);
     if (lane == 0) {
       uint8_t* st = wbase + s * Cfg::STAGE;
       const int row = pb * BS + (u % SUB) * kTB;
@@ -191,7 +190,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   int u = 0;
   for (; u < nunit; ++u) {
     const int s = u % kStages;
-    if (!__all_sync(kFull, mbar_wait(&bars[s], (u / kStages) & 1))) break;
+    if (!__all_sync(kPfxFull, mbar_wait(&bars[s], (u / kStages) & 1))) break;
     const uint32_t kb = smem_u32(wbase + s * Cfg::STAGE);
     const uint32_t vb = kb + Cfg::TILE;
 
@@ -209,8 +208,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float mx = fmaxf(fmaxf(sc[0][2 * i], sc[0][2 * i + 1]), fmaxf(sc[1][2 * i], sc[1][2 * i + 1]));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(kPfxFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kPfxFull, mx, 2));
       const float m_new = fmaxf(mrow[i], mx * sl2);
       alpha[i] = fast_exp2(mrow[i] - m_new);
       mrow[i] = m_new;
@@ -223,8 +222,8 @@ __global__ void __launch_bounds__(kWarps * 32)
           pr[nt][2 * i + e] = p;
           sum += p;
         }
-      sum += __shfl_xor_sync(kFull, sum, 1);
-      sum += __shfl_xor_sync(kFull, sum, 2);
+      sum += __shfl_xor_sync(kPfxFull, sum, 1);
+      sum += __shfl_xor_sync(kPfxFull, sum, 2);
       lrow[i] = lrow[i] * alpha[i] + sum;
     }
 #pragma unroll
@@ -254,7 +253,6 @@ __global__ void __launch_bounds__(kWarps * 32)
       issue(nxt, s);
     }
   }
-  pdl_launch_dependents();  // the suffix partitions may be scheduled now
   if (u < nunit) {
     if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
     for (int j = u; j < nunit && j < u + kStages; ++j)
@@ -287,46 +285,6 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-template <int D, int BS>
-cudaError_t launch_prefix_t(const DecodeArgs& a, const CUtensorMap& kmap,
-                            const CUtensorMap& vmap, cudaStream_t stream) {
-  using Cfg = PrefixCfg<D>;
-  auto kern = prefix_kernel<D, BS>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_groups, (a.H + kWarps - 1) / kWarps, a.max_prefix_parts);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = Cfg::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
-}
 
-}  // namespace
-
-bool prefix_supported(int D, int block_size, int max_group_size) {
-  return (D == 64 || D == 128) && (block_size == 16 || block_size == 32) &&
-         max_group_size >= 1 && max_group_size <= kMaxMembers;
-}
-
-cudaError_t launch_prefix(const DecodeArgs& a, const CUtensorMap& kmap_sw,
-                          const CUtensorMap& vmap_sw, cudaStream_t stream) {
-  if (a.num_groups <= 0 || a.max_prefix_parts <= 0) return cudaSuccess;
-  if (a.D == 128 && a.block_size == 16) return launch_prefix_t<128, 16>(a, kmap_sw, vmap_sw, stream);
-  if (a.D == 128 && a.block_size == 32) return launch_prefix_t<128, 32>(a, kmap_sw, vmap_sw, stream);
-  if (a.D == 64 && a.block_size == 16) return launch_prefix_t<64, 16>(a, kmap_sw, vmap_sw, stream);
-  if (a.D == 64 && a.block_size == 32) return launch_prefix_t<64, 32>(a, kmap_sw, vmap_sw, stream);
-  return cudaErrorInvalidValue;
-}
-
+}  // namespace pfx
 }  // namespace pk
