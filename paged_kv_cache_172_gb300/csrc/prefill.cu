@@ -228,10 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and K_t landed; O_X (+)= P_X(t) V_t once P_X(t) is stored and V_t
     // landed.  Each thread's commits track its own MMAs, and K is read only
     // by the first, V and O only by the second.
-    if (lane == 0) {
-      const int nt[2] = {ntile_a, ntile_b};
-      auto landed = [&](int u) { return mbar_wait(&kv_full[u % kStages], (u / kStages) & 1); };
-      if (warp == kWarpMma) {
+    const int nt[2] = {ntile_a, ntile_b};
+    auto landed = [&](int u) { return mbar_wait(&kv_full[u % kStages], (u / kStages) & 1); };
+    if (warp == kWarpMma) {
+      if (lane == 0) {
         // Base descriptors; each MMA adds a compile-time offset (a slot, a
         // tile or a K step never carries out of the 14-bit address field).
         const uint64_t dq = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128B);
@@ -254,26 +254,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (ok) tc::commit(&kv_empty[u % kStages]);  // K_t has no further reader
         }
-      } else {
-        const uint64_t dp = tc::smem_desc(smem_u32(sP), 16, 1024, tc::kSwizzle128B);
-        const uint64_t dv = tc::smem_desc(smem_u32(sKV), kSlabBytes, 1024, tc::kSwizzle128B);
-        for (int t = 0; t < n_kv && ok; ++t) {
-          const int u = load_v(t, n_kv);
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (t >= nt[x]) continue;
-            if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
-            if (!(ok = landed(u))) break;
-            tc::fence_after_sync();
-            const uint64_t da = dp + x * kTileDesc;
-            const uint64_t db = dv + (u % kStages) * kTileDesc;
+      }
+    } else {
+      const uint64_t dp = tc::smem_desc(smem_u32(sP), 16, 1024, tc::kSwizzle128B);
+      const uint64_t dv = tc::smem_desc(smem_u32(sKV), kSlabBytes, 1024, tc::kSwizzle128B);
+      // Rows of the last key tile at or past the context length come from the
+      // unused tail of the last block (never written: possibly NaN) and would
+      // give P * V = 0 * NaN; the whole warp zeroes them once V has landed.
+      const int tail_rows = n - (n_kv - 1) * kTileN;  // valid rows of the last key tile
+      auto issue_pv = [&](int t) {  // lane 0
+        const int u = load_v(t, n_kv);
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (t >= nt[x]) continue;
+          if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
+          if (!(ok = landed(u))) break;
+          tc::fence_after_sync();
+          const uint64_t da = dp + x * kTileDesc;
+          const uint64_t db = dv + (u % kStages) * kTileDesc;
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              tc::mma_f16(tmem + kColO + x * kD, da + kmajor_off(kk), db + vmn_off(kk), kIdescO,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-            tc::commit(&pv_done[x]);
-          }
-          if (ok) tc::commit(&kv_empty[u % kStages]);  // V_t has no further reader
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            tc::mma_f16(tmem + kColO + x * kD, da + kmajor_off(kk), db + vmn_off(kk), kIdescO,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(&pv_done[x]);
         }
+        if (ok) tc::commit(&kv_empty[u % kStages]);  // V_t has no further reader
+      };
+      if (lane == 0)
+        for (int t = 0; t + 1 < n_kv && ok; ++t) issue_pv(t);
+      ok = __shfl_sync(kFull, ok, 0);
+      if (ok && n_kv > 0) {
+        if (tail_rows < kTileN) {
+          const int u = load_v(n_kv - 1, n_kv);
+          if (lane == 0) ok = landed(u);
+          ok = __shfl_sync(kFull, ok, 0);
+          if (ok) {
+            uint8_t* vt = sKV + (u % kStages) * kTileBytes;
+            for (int i = lane; i < (kTileN - tail_rows) * 16; i += 32) {  // 16 chunks per row
+              const int r = tail_rows + (i >> 4), c = i & 15;
+              *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + r * 128 + (c & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // read by the tensor core (async proxy)
+          }
+          __syncwarp();
+        }
+        if (ok && lane == 0) issue_pv(n_kv - 1);
       }
     }
     ok = __shfl_sync(kFull, ok, 0);
