@@ -88,7 +88,9 @@ int pa_version(void);
  *     out[b,h,:] = sum_j p_j * v_cache[blk(j), j % bs, h, :]
  * for j in [0, n).  n == 0 gives a zero row.  Only the first
  * ceil(n / block_size) entries of a table row are read; later entries may
- * hold anything (conventionally -1).
+ * hold anything (conventionally -1).  Pool slots past a sequence's length
+ * (the tail of its last block, unreferenced blocks) may hold anything, NaN
+ * included, without changing the result.
  *
  * q            [B, H, D] fp16
  * k_cache      [num_blocks, block_size, H, D] fp16 (v_cache alike)
@@ -265,7 +267,8 @@ pa_status pa_decode_static(const pa_half *q, const pa_half *k_cache,
  * K/V must already be in the cache), and attends to keys
  * 0 .. n - Lq + i (causal mask aligned to the end of the context; with
  * Lq == n this is the lower-triangular mask of the blog's sec. 3.2.2, with
- * Lq == 1 it is decode).  Same per-row arithmetic as pa_decode.
+ * Lq == 1 it is decode).  Same per-row arithmetic as pa_decode; pool slots
+ * past a sequence's length may hold anything, NaN included.
  *
  * q   [B, H, Lq, D] fp16 (the blog's [batch, heads, seq_len, head_dim])
  * out [B, H, Lq, D] fp16
