@@ -61,6 +61,19 @@ struct LaneVec<4> {
   }
 };
 template <>
+struct LaneVec<8> {
+  uint4 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void to_float(float* f) const {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = a.x; f[2 * i + 1] = a.y;
+    }
+  }
+};
+template <>
 struct LaneVec<2> {
   uint32_t raw;
   __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
@@ -86,7 +99,19 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c) {
 // Lane partial of q . k for EPL e4m3 codes of k (fp16 query pairs qh).
 template <int EPL>
 __device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) {
-  if constexpr (EPL == 4) {
+  if constexpr (EPL == 8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const uint32_t w[2] = {raw.x, raw.y};
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+      t = fma2_f16_f32(qh[2 * i], *reinterpret_cast<const uint32_t*>(&lo), t);
+      t = fma2_f16_f32(qh[2 * i + 1], *reinterpret_cast<const uint32_t*>(&hi), t);
+    }
+    return t;
+  } else if constexpr (EPL == 4) {
     const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
@@ -104,7 +129,10 @@ __device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) 
 template <int EPL>
 __device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint8_t* p) {
   const uint16_t wb = __half_as_ushort(w);
-  if constexpr (EPL == 4) {
+  if constexpr (EPL == 8) {
+    axpy_e4m3<4>(o, w, p);
+    axpy_e4m3<4>(o + 4, w, p + 4);
+  } else if constexpr (EPL == 4) {
     const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
@@ -127,7 +155,15 @@ __device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint8_t* p) 
 
 template <int EPL>
 __device__ __forceinline__ void store_half_row(__half* dst, const float* v) {
-  if constexpr (EPL == 4) {
+  if constexpr (EPL == 8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h2 = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (EPL == 4) {
     __half2 a = __floats2half2_rn(v[0], v[1]);
     __half2 b = __floats2half2_rn(v[2], v[3]);
     uint2 u;
@@ -153,7 +189,11 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
 
 template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
 struct PartitionCfg {
-  static constexpr int EPL = D / 32;                  // dims per lane
+  // Lanes covering one token's D dims: 32 for fp16, 16 for e4m3 (two tokens
+  // per warp instruction, halving the shuffles per byte of the slimmer rows).
+  static constexpr int RL = FP8 ? 16 : 32;
+  static constexpr int NT = 32 / RL;                  // tokens per warp instruction
+  static constexpr int EPL = D / RL;                  // dims per lane
   static constexpr int TB = BS < 16 ? BS : 16;        // tokens per TMA box / pipeline stage
   static constexpr int SUB = BS / TB;                 // stages per physical block
   static constexpr int ELEM = FP8 ? 1 : 2;            // bytes per stored K/V element
@@ -178,6 +218,9 @@ __global__ void __launch_bounds__(WARPS * 32)
   constexpr int TB = Cfg::TB;
   constexpr int SUB = Cfg::SUB;
   constexpr int LPT = Cfg::LANES_PER_TOKEN;
+  constexpr int RL = Cfg::RL, NT = Cfg::NT;
+  constexpr int ITER = TB / NT;  // warp instructions per stage (one token per RL lanes each)
+  static_assert(ITER >= 1 && RL % ITER == 0, "stage tokens vs row lanes");
   static_assert(BS >= 1 && BS <= 32 && (32 % BS) == 0, "block_size must divide 32");
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -214,7 +257,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
   if (tok0 >= ctx) {
-    if (part == 0) {  // empty sequence: zero row
+    if (part == 0 && lane < RL) {  // empty sequence: zero row
       float z[EPL] = {};
       store_half_row<EPL>(a.out + row_bh * D + lane * EPL, z);
     }
@@ -235,16 +278,18 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
 
+  // Dims [dl, dl + EPL) of this lane; lane / RL picks the token of a pair.
+  const int dl = (lane % RL) * EPL;
   // Query slice of this lane (and, for e4m3 pools, its fp16 pairs).
   float qf[EPL];
   uint32_t qh[EPL / 2];
   {
     LaneVec<EPL> qv;
-    qv.load(a.q + row_bh * D + lane * EPL);
+    qv.load(a.q + row_bh * D + dl);
     qv.to_float(qf);
 #pragma unroll
     for (int e = 0; e < EPL / 2; ++e)
-      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + lane * EPL)[e];
+      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + dl)[e];
   }
 
   if (lane == 0) {
@@ -277,7 +322,8 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
   for (int e = 0; e < EPL; ++e) o[e] = 0.f;
 
-  const int my_tok = lane / LPT;  // token whose score this lane holds after the butterfly
+  // Token whose score this lane holds after the butterfly (lane / LPT for RL = 32).
+  const int my_tok = ((lane % RL) / (RL / ITER)) * NT + lane / RL;
   int i = 0;
   for (; i < nunit; ++i) {
     const int s = i % NSTAGE;
@@ -314,26 +360,28 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
     }
 
-    // Partial dot products of every token of the block.
-    float part_dot[TB];
+    // Partial dot products: instruction it covers token it * NT + lane / RL.
+    float part_dot[ITER];
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
+    for (int it = 0; it < ITER; ++it) {
+      const int t = it * NT + lane / RL;
       if constexpr (FP8) {
-        part_dot[t] = dot_e4m3<EPL>(qh, kst + t * D + lane * EPL);
+        part_dot[it] = dot_e4m3<EPL>(qh, kst + t * D + dl);
       } else {
         float kf[EPL];
         LaneVec<EPL> kv;
-        kv.load(ks + t * D + lane * EPL);
+        kv.load(ks + t * D + dl);
         kv.to_float(kf);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
-        part_dot[t] = acc;
+        part_dot[it] = acc;
       }
     }
-    // Transposing butterfly: after round r, lanes keep half of the tokens.
+    // Transposing butterfly over the RL lanes of a token: after round r,
+    // lanes keep half of the remaining instructions' tokens.
 #pragma unroll
-    for (int cnt = TB, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+    for (int cnt = ITER, off = RL / 2; cnt > 1; cnt >>= 1, off >>= 1) {
       const bool upper = (lane & off) != 0;
 #pragma unroll
       for (int k = 0; k < cnt / 2; ++k) {
@@ -344,7 +392,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     // Remaining lanes of the same token hold disjoint dim ranges: sum them.
 #pragma unroll
-    for (int off = LPT / 2; off >= 1; off >>= 1)
+    for (int off = RL / ITER / 2; off >= 1; off >>= 1)
       part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
 
     float dot = part_dot[0];
@@ -364,18 +412,23 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
     // e4m3 pools: the weight p * v_scale goes to fp16 (relative error 2^-11)
     // times 2^8, which keeps it in the normal fp16 range; o carries the 2^8
-    // until the partition writes it.
-    const float pr_v = FP8 ? pr * 256.f : pr;
+    // until the partition writes it.  The lane holding a token's score forms
+    // its weight; instruction it broadcasts the weights of its NT tokens.
+    float wv = pr;
+    if constexpr (FP8) wv = __uint_as_float((uint32_t)__half_as_ushort(
+                           __float2half_rn(pr * 256.f * vscl[my_tok])));
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
-      const float pt = __shfl_sync(kFull, pr_v, t * LPT);
+    for (int it = 0; it < ITER; ++it) {
+      const int t = it * NT + lane / RL;
+      const float pt = __shfl_sync(kFull, wv, (lane / RL) * RL + it * (RL / ITER));
       if (t < valid) {
         if constexpr (FP8) {
-          axpy_e4m3<EPL>(o, __float2half_rn(pt * vscl[t]), kst + Cfg::TILE_BYTES + t * D + lane * EPL);
+          axpy_e4m3<EPL>(o, __ushort_as_half((unsigned short)__float_as_uint(pt)),
+                         kst + Cfg::TILE_BYTES + t * D + dl);
         } else {
           float vf[EPL];
           LaneVec<EPL> vv;
-          vv.load(vs + t * D + lane * EPL);
+          vv.load(vs + t * D + dl);
           vv.to_float(vf);
 #pragma unroll
           for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
@@ -406,20 +459,29 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= 1.f / 256.f;  // exact
   }
+  if constexpr (RL < 32) {  // the two halves accumulated different tokens
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], 16);
+  }
   const int n_parts = (ctx + a.part_tokens - 1) / a.part_tokens;
   if (n_parts == 1) {
     const float inv = 1.f / l;
     float r[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) r[e] = o[e] * inv;
-    store_half_row<EPL>(a.out + row_bh * D + lane * EPL, r);
+    if (lane < RL) store_half_row<EPL>(a.out + row_bh * D + dl, r);
   } else {
     const size_t row = row_bh * a.num_parts + part;
-    float* dst = a.ws_o + row * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-    } else {
-      *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+    float* dst = a.ws_o + row * D + dl;
+    if (lane < RL) {
+      if constexpr (EPL == 8) {
+        *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      } else if constexpr (EPL == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+      } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+      }
     }
     if (lane == 0) *reinterpret_cast<float2*>(a.ws_ml + row * 2) = make_float2(m, l);
   }

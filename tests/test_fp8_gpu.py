@@ -73,7 +73,7 @@ def test_fp8_write_bit_exact(D, bs):
     assert np.array_equal(g[2].cpu().numpy(), rks) and np.array_equal(g[3].cpu().numpy(), rvs)
 
 
-@pytest.mark.parametrize("D,bs", [(128, 16), (64, 16), (128, 32), (128, 4)])
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 16), (128, 32), (128, 4), (128, 8), (64, 4), (64, 8), (64, 32)])
 def test_fp8_decode_parity_and_accuracy(D, bs):
     ctx = [1, bs, bs + 1, 70, 333, 1024]
     batch = workloads.random_decode(len(ctx), 4, D, bs, ctx, seed=90 + D + bs, device="cpu")
