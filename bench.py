@@ -520,6 +520,8 @@ def run_aux(args, name):
         out = torch.empty_like(batch.q)
         B, H, Lq, D = batch.q.shape
         bs = batch.block_size
+        pws = pk.pa_prefill_workspace_size(B, H, Lq, D)
+        prefill_ws = torch.empty(max(pws // 4, 1) + 4, dtype=torch.float32, device=dev)
         phases = [
             ("kv_cache_write", lambda: pk.pa_kv_cache_write(batch.k_new, batch.v_new,
                                                             batch.slot_mapping, batch.k_cache,
@@ -527,8 +529,8 @@ def run_aux(args, name):
                                                             stream=stream)),
             ("prefill", lambda: pk.pa_prefill_chunk(batch.q, batch.k_cache, batch.v_cache,
                                                     batch.block_tables, batch.context_lens,
-                                                    batch.scale, out=out, status=status,
-                                                    stream=stream)),
+                                                    batch.scale, out=out, workspace=prefill_ws,
+                                                    status=status, stream=stream)),
         ]
         work = prefill_flops(ctx, Lq, H, D)
         main, unit, bound = "prefill", "TFLOP/s", "tensor"

@@ -275,12 +275,23 @@ pa_status pa_decode_static(const pa_half *q, const pa_half *k_cache,
  * context_lens[b] in [Lq, max_blocks_per_seq * block_size]; scale > 0.
  * D == 128 and block_size in {16, 32} run on the tcgen05 tensor-core kernel;
  * other supported (D, block_size) pairs return PA_ERR_UNSUPPORTED.
+ *
+ * workspace (device, 16-byte aligned, caller-owned, may be NULL): with at
+ * least pa_prefill_workspace_size(B, H, Lq, D) bytes, the work units of the
+ * grid's last, partial round (one CTA per SM) are each split into key ranges
+ * whose partial results are merged by log-sum-exp, so that round fills the
+ * GPU; with NULL every unit runs whole (same result up to rounding).  A
+ * non-NULL workspace smaller than that returns PA_ERR_WORKSPACE.  The size
+ * depends on the SM count of the current device.
  * ------------------------------------------------------------------------- */
+size_t pa_prefill_workspace_size(int B, int H, int Lq, int D);
+
 pa_status pa_prefill_chunk(const pa_half *q, const pa_half *k_cache,
                            const pa_half *v_cache, const int32_t *block_tables,
                            const int32_t *context_lens, int B, int H, int Lq,
                            int D, int block_size, int num_blocks,
                            int max_blocks_per_seq, float scale, pa_half *out,
+                           void *workspace, size_t workspace_bytes,
                            int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------

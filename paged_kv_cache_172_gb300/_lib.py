@@ -23,7 +23,8 @@ PA_DEV_TIMEOUT = 0x10
 EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
-    "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy", "pa_decode_static",
+    "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
+    "pa_decode_static",
     "pa_decode_append", "pa_decode_shared_prefix", "pa_kv_cache_write_fp8", "pa_decode_fp8",
 )
 
@@ -57,8 +58,10 @@ def _bind(lib):
     lib.pa_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                               ctypes.c_float, _P, _P, _SZ, _P, _P]
     lib.pa_decode.restype = _I
+    lib.pa_prefill_workspace_size.argtypes = [_I, _I, _I, _I]
+    lib.pa_prefill_workspace_size.restype = _SZ
     lib.pa_prefill_chunk.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
-                                     ctypes.c_float, _P, _P, _P]
+                                     ctypes.c_float, _P, _P, _SZ, _P, _P]
     lib.pa_prefill_chunk.restype = _I
     lib.pa_kv_cache_write.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.pa_kv_cache_write.restype = _I
@@ -297,10 +300,18 @@ def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context
     return out
 
 
+def pa_prefill_workspace_size(B, H, Lq, D):
+    """Bytes of workspace pa_prefill_chunk uses to split the grid's last round
+    (0 when it needs none) on the current device."""
+    return int(lib().pa_prefill_workspace_size(int(B), int(H), int(Lq), int(D)))
+
+
 def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-                     status=None, stream=None):
+                     workspace=None, tail_split=True, status=None, stream=None):
     """Chunked prefill attention.  q [B,H,Lq,D] fp16 are the last Lq positions
-    of each sequence (end-aligned causal mask).  Returns out [B,H,Lq,D]."""
+    of each sequence (end-aligned causal mask).  Returns out [B,H,Lq,D].
+    A workspace for the tail split is allocated when not given; tail_split=False
+    passes none (every work unit runs whole)."""
     _need(q, torch.float16, "q", 4)
     _need(k_cache, torch.float16, "k_cache", 4)
     _need(v_cache, torch.float16, "v_cache", 4)
@@ -314,10 +325,17 @@ def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out
         out = torch.empty_like(q)
     else:
         _need(out, torch.float16, "out", 4)
+    if not tail_split:
+        workspace = None
+    elif workspace is None:
+        ws_bytes = pa_prefill_workspace_size(B, H, Lq, D) if B * Lq > 0 else 0
+        if ws_bytes > 0:
+            workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                 _ptr(context_lens), B, H, Lq, D, bs, NB,
-                                block_tables.shape[1], float(scale), _ptr(out), _ptr(status),
-                                _stream(stream, q.device))
+                                block_tables.shape[1], float(scale), _ptr(out), _ptr(workspace),
+                                ws_len, _ptr(status), _stream(stream, q.device))
     _check(rc, "pa_prefill_chunk")
     return out
 

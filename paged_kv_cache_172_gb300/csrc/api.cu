@@ -384,10 +384,16 @@ pa_status pa_decode_append(const pa_half* q, const pa_half* k_new, const pa_half
 // ---------------------------------------------------------------------------
 // chunked prefill
 // ---------------------------------------------------------------------------
+size_t pa_prefill_workspace_size(int B, int H, int Lq, int D) {
+  if (D != 128) return 0;
+  return pk::prefill_workspace_bytes(B, H, Lq);
+}
+
 pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
                            const int32_t* block_tables, const int32_t* context_lens, int B, int H,
                            int Lq, int D, int block_size, int num_blocks, int max_blocks_per_seq,
-                           float scale, pa_half* out, int32_t* status, pa_stream_t stream) {
+                           float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+                           int32_t* status, pa_stream_t stream) {
   if (B < 0 || H <= 0 || Lq < 0 || max_blocks_per_seq <= 0 || !isfinite(scale) ||
       !(scale > 0.f))
     return PA_ERR_INVALID;
@@ -398,8 +404,13 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
     return PA_ERR_INVALID;
   if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
   if ((long long)Lq > (long long)max_blocks_per_seq * block_size) return PA_ERR_INVALID;
+  const size_t need = pk::prefill_workspace_bytes(B, H, Lq);
+  if (workspace != nullptr && need > 0 && workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (workspace != nullptr && !aligned16(workspace)) return PA_ERR_INVALID;
   pk::PrefillArgs a;
   a.q = reinterpret_cast<const __half*>(q);
+  a.ws = reinterpret_cast<float*>(workspace);
+  a.ws_floats = workspace != nullptr ? workspace_bytes / sizeof(float) : 0;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = reinterpret_cast<__half*>(out);

@@ -85,6 +85,14 @@ cudaError_t launch_block_copy(__half* kc, __half* vc, const int64_t* pairs, int 
 
 struct PrefillArgs {
   const __half* q;
+  // Tail split (set by launch_prefill): CTAs [0, full_units) are whole units
+  // (one per (sequence, head, 256-query pair), in that order, units gx * H * B);
+  // each later unit's key tiles are split into `split` parts whose partials
+  // (kPrefillPartialStride floats per query row) go to ws and are merged by a
+  // combine kernel.
+  float* ws;
+  size_t ws_floats;
+  int gx, full_units, split;
   const int32_t* block_tables;
   const int32_t* context_lens;
   __half* out;
@@ -92,7 +100,10 @@ struct PrefillArgs {
   int B, H, Lq, D, block_size, num_blocks, max_blocks;
   float scale_log2;
 };
+constexpr int kPrefillPartialStride = 132;  // o[128], m, l, pad (16-byte aligned rows)
 bool prefill_supported(int D, int block_size);
+// Bytes of workspace the tail split needs on the current device (0: none).
+size_t prefill_workspace_bytes(int B, int H, int Lq);
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                            cudaStream_t stream);
 

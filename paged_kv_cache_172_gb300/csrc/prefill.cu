@@ -115,7 +115,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ct = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // Work unit (sequence, head, 256-query pair) and, for a split unit, its part.
+  int unit = blockIdx.x, part = -1;
+  if (unit >= a.full_units) {
+    const int t = unit - a.full_units;
+    unit = a.full_units + t / a.split;
+    part = t % a.split;
+  }
+  const int ct = unit % a.gx, h = (unit / a.gx) % a.H, b = unit / (a.gx * a.H);
+  // Partial rows of this part (query row r of the unit at ws_part + r * stride).
+  float* ws_part = part < 0 ? nullptr
+                            : a.ws + ((size_t)(unit - a.full_units) * a.split + part) *
+                                         (2 * kTileM) * kPrefillPartialStride;
 
   pdl_wait();  // inputs may come from the previous kernel on the stream
   const int n = a.context_lens[b];
@@ -123,10 +134,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_all = min(2 * kTileM, a.Lq - q0);
   const size_t out_row0 = ((size_t)b * a.H + h) * a.Lq + q0;
   if (n < a.Lq || n > a.max_blocks * BS) {
-    if (threadIdx.x == 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
-    uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * kD);
-    for (int i = threadIdx.x; i < rows_all * (kD / 8); i += kThreads)
-      o4[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0 && part <= 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+    if (part < 0) {
+      uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * kD);
+      for (int i = threadIdx.x; i < rows_all * (kD / 8); i += kThreads)
+        o4[i] = make_uint4(0, 0, 0, 0);
+    } else {  // an empty partial: the combine writes zero rows
+      for (int r = threadIdx.x; r < 2 * kTileM; r += kThreads) {
+        ws_part[(size_t)r * kPrefillPartialStride + kD] = -INFINITY;
+        ws_part[(size_t)r * kPrefillPartialStride + kD + 1] = 0.f;
+      }
+    }
     return;
   }
   // Per Q tile (A = 0, B = 1): rows, sequence position of row 0, key tiles.
@@ -135,9 +153,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_b = max(0, min(kTileM, a.Lq - (q0 + kTileM)));
   const int pos0_a = n - a.Lq + q0;
   const int pos0_b = pos0_a + kTileM;
-  const int ntile_a = (pos0_a + rows_a - 1) / kTileN + 1;
-  const int ntile_b = rows_b > 0 ? (pos0_b + rows_b - 1) / kTileN + 1 : 0;
-  const int n_kv = max(ntile_a, ntile_b);
+  // Key tiles of the unit, then this CTA's range [kt0, kt0 + n_kv) of them;
+  // ntile_a / ntile_b count the range's tiles each Q tile reads.
+  const int ntile_a_all = (pos0_a + rows_a - 1) / kTileN + 1;
+  const int ntile_b_all = rows_b > 0 ? (pos0_b + rows_b - 1) / kTileN + 1 : 0;
+  const int n_kv_all = max(ntile_a_all, ntile_b_all);
+  int kt0 = 0, n_kv = n_kv_all;
+  if (part >= 0) {
+    kt0 = part * n_kv_all / a.split;
+    n_kv = (part + 1) * n_kv_all / a.split - kt0;
+  }
+  const int ntile_a = min(max(ntile_a_all - kt0, 0), n_kv);
+  const int ntile_b = min(max(ntile_b_all - kt0, 0), n_kv);
   const int nblk_seq = (n + BS - 1) / BS;
 
   if (threadIdx.x == 0) {
@@ -182,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Key tile t (K when v == 0, else V) into ring slot u % kStages.
     auto load_tile = [&](int t, int v, int u) {
-      const int lb0 = t * BPT;
+      const int lb0 = (kt0 + t) * BPT;
       if (lb0 < win || lb0 + BPT > win + kTblWindow) {
         // K_t is requested before V_{t-1}: start the window one tile early.
         win = (v == 0 && t > 0) ? lb0 - BPT : lb0;
@@ -261,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Rows of the last key tile at or past the context length come from the
       // unused tail of the last block (never written: possibly NaN) and would
       // give P * V = 0 * NaN; the whole warp zeroes them once V has landed.
-      const int tail_rows = n - (n_kv - 1) * kTileN;  // valid rows of the last key tile
+      const int tail_rows = n - (kt0 + n_kv - 1) * kTileN;  // valid rows of the last key tile
       auto issue_pv = [&](int t) {  // lane 0
         const int u = load_v(t, n_kv);
         for (int x = 0; x < 2 && ok; ++x) {
@@ -320,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntile && ok; ++j) {
       if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
-      const int kbase = j * kTileN;
+      const int kbase = (kt0 + j) * kTileN;
       const bool diag = kbase + kTileN - 1 > pos0;  // some key here is past some row
       // The whole S row in registers; S_X is then free for S_X(j+1).
       uint32_t r[4][32];
@@ -402,7 +429,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[x]);
     }
     if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&pv_done[x], (ntile - 1) & 1));
-    if (ok && ntile > 0) {
+    if (ok && part >= 0) {
+      // Part of a split unit: the unnormalised row (o, m, l) for the combine;
+      // a Q tile with no key tile in this part leaves an empty partial.
+      float* wrow = ws_part + (size_t)(x * kTileM + row) * kPrefillPartialStride;
+      if (ntile > 0) tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        if (ntile > 0) {
+          tc::ld_32x32(t_o + c * 32, o);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        float4* dst = reinterpret_cast<float4*>(wrow + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                               __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+      }
+      wrow[kD] = ntile > 0 ? m : -INFINITY;
+      wrow[kD + 1] = ntile > 0 ? l : 0.f;
+    } else if (ok && ntile > 0) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
       __half* orow = a.out + (out_row0 + x * kTileM + row) * kD;
@@ -451,9 +501,94 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merge the parts of split units by log-sum-exp (m, l in the softmax's log2
+// domain): one warp per query row, lane l owns dims [4l, 4l + 4).
+__global__ void __launch_bounds__(256)
+    prefill_combine_kernel(const PrefillArgs a, int n_split_units) {
+  pdl_wait();  // the partials come from the prefill kernel just before
+  const int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= n_split_units * 2 * kTileM) return;
+  const int su = w / (2 * kTileM), r = w % (2 * kTileM);
+  const int unit = a.full_units + su;
+  const int ct = unit % a.gx, h = (unit / a.gx) % a.H, b = unit / (a.gx * a.H);
+  const int qi = ct * 2 * kTileM + r;
+  if (qi >= a.Lq) return;
+  const float* base = a.ws + (size_t)su * a.split * (2 * kTileM) * kPrefillPartialStride +
+                      (size_t)r * kPrefillPartialStride;
+  const size_t part_stride = (size_t)(2 * kTileM) * kPrefillPartialStride;
+  float M = -INFINITY;
+  for (int s = 0; s < a.split; ++s) {
+    const float* pr = base + s * part_stride;
+    if (pr[kD + 1] > 0.f) M = fmaxf(M, pr[kD]);
+  }
+  float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < a.split; ++s) {
+    const float* pr = base + s * part_stride;
+    const float ls = pr[kD + 1];
+    if (ls > 0.f) {
+      const float wgt = ex2_approx(pr[kD] - M);
+      L += ls * wgt;
+      const float4 v = *reinterpret_cast<const float4*>(pr + lane * 4);
+      o[0] += wgt * v.x; o[1] += wgt * v.y; o[2] += wgt * v.z; o[3] += wgt * v.w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __half2 h0 = __floats2half2_rn(o[0] * inv, o[1] * inv);
+  __half2 h1 = __floats2half2_rn(o[2] * inv, o[3] * inv);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&h0);
+  u.y = *reinterpret_cast<uint32_t*>(&h1);
+  *reinterpret_cast<uint2*>(a.out + (((size_t)b * a.H + h) * a.Lq + qi) * kD + lane * 4) = u;
+}
+
+int sm_count() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached = n;
+  }
+  return cached;
+}
+
+// Tail split plan: the units of the last, partial round of the grid (one CTA
+// per SM) are cut into `split` key ranges so that round fills the SMs.
+struct SplitPlan {
+  int units, full_units, split;
+};
+SplitPlan split_plan(int B, int H, int Lq) {
+  SplitPlan p;
+  const int gx = (Lq + 2 * kTileM - 1) / (2 * kTileM);
+  p.units = gx * H * B;
+  p.full_units = p.units;
+  p.split = 1;
+  const int nsm = sm_count();
+  if (nsm <= 0 || p.units <= nsm) return p;
+  const int rem = p.units % nsm;
+  if (rem == 0) return p;
+  const int s = min(4, nsm / rem);
+  if (s < 2) return p;
+  p.full_units = p.units - rem;
+  p.split = s;
+  return p;
+}
+
 template <int BS>
-cudaError_t launch_prefill_t(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const void* v_cache,
                              cudaStream_t stream) {
+  PrefillArgs a = a_in;
+  a.gx = (a.Lq + 2 * kTileM - 1) / (2 * kTileM);
+  SplitPlan plan = split_plan(a.B, a.H, a.Lq);
+  const size_t need = (size_t)(plan.units - plan.full_units) * plan.split * (2 * kTileM) *
+                      kPrefillPartialStride;
+  if (plan.split > 1 && (a.ws == nullptr || a.ws_floats < need)) {
+    plan.full_units = plan.units;  // no workspace: every unit whole
+    plan.split = 1;
+  }
+  a.full_units = plan.full_units;
+  a.split = plan.split;
   CUtensorMap qmap, kmap, vmap;
   const long long rows = (long long)a.num_blocks * BS;
   cudaError_t e;
@@ -485,7 +620,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const void* k_cache, const vo
     attr_done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Lq + 2 * kTileM - 1) / (2 * kTileM), a.H, a.B);
+  cfg.gridDim = dim3(plan.full_units + (plan.units - plan.full_units) * plan.split);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -494,10 +629,26 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const void* k_cache, const vo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
+  e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
+  if (e != cudaSuccess || plan.split == 1) return e;
+  const int n_split = plan.units - plan.full_units;
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3((n_split * 2 * kTileM * 32 + 255) / 256);
+  cc.blockDim = dim3(256);
+  cc.stream = stream;
+  cc.attrs = attr;
+  cc.numAttrs = 1;
+  return cudaLaunchKernelEx(&cc, prefill_combine_kernel, a, n_split);
 }
 
 }  // namespace
+
+size_t prefill_workspace_bytes(int B, int H, int Lq) {
+  if (B <= 0 || H <= 0 || Lq <= 0) return 0;
+  const SplitPlan p = split_plan(B, H, Lq);
+  return (size_t)(p.units - p.full_units) * p.split * (2 * kTileM) * kPrefillPartialStride *
+         sizeof(float);
+}
 
 bool prefill_supported(int D, int block_size) {
   return D == kD && (block_size == 16 || block_size == 32);

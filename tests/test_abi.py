@@ -103,14 +103,14 @@ def test_copy_validation(lib):
 
 def test_prefill_validation(lib):
     rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 64, 4, 8, 4,
-                              0.1, 0x1000, NULL, NULL)
+                              0.1, 0x1000, NULL, 0, NULL, NULL)
     assert rc == pk.PA_ERR_UNSUPPORTED  # (D=64, bs=4) has no tensor-core kernel
     rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, -2, 4, 8, 128, 16, 8, 4,
-                              0.1, 0x1000, NULL, NULL)
+                              0.1, 0x1000, NULL, 0, NULL, NULL)
     assert rc == pk.PA_ERR_INVALID
     for bad_scale in (0.0, -0.5, float("inf")):  # the prefill kernel needs scale > 0
         rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 128, 16, 8,
-                                  4, bad_scale, 0x1000, NULL, NULL)
+                                  4, bad_scale, 0x1000, NULL, 0, NULL, NULL)
         assert rc == pk.PA_ERR_INVALID
 
 

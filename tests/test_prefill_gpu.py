@@ -138,3 +138,31 @@ def test_chunked_prefill_workload():
     err = np.concatenate(errs)
     print(f"chunked prefill: {len(errs)} rows, max|err| {err.max():.2e} mean {err.mean():.2e}")
     assert err.max() <= 5e-3 and err.mean() <= 5e-4
+
+
+def test_tail_split_matches_whole_units_and_oracle():
+    # One sequence, H = SMs + 8 heads, 256 queries: one work unit per head, so
+    # the last 8 heads form the partial last round and are split into key ranges.
+    nsm = torch.cuda.get_device_properties(DEV).multi_processor_count
+    H, Lq, bs = nsm + 8, 256, 16
+    ctx = [Lq + 5 * 128 + 37]
+    assert pk.pa_prefill_workspace_size(1, H, Lq, 128) > 0
+    batch = workloads.random_prefill(1, H, 128, bs, Lq, ctx, seed=95, device="cpu",
+                                     write_chunk=False)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out_split = run_prefill(g, batch.scale, status=status)  # the binding allocates the workspace
+    out_whole = pk.pa_prefill_chunk(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                    g["context_lens"], batch.scale, tail_split=False,
+                                    status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # the split heads against the oracle (heads sliced out of the pool)
+    hs = list(range(H - 10, H))
+    sl = lambda t: t[:, :, hs].contiguous()
+    ref = oracle.prefill(batch.q[:, hs].contiguous().numpy(), sl(batch.k_cache).numpy(),
+                         sl(batch.v_cache).numpy(), batch.block_tables.numpy(),
+                         batch.context_lens.numpy(), batch.scale)
+    assert_close(out_split[:, hs], ref, what="tail-split heads")
+    e = errors(out_split, out_whole.float().cpu().numpy().astype(np.float64))
+    assert e[0] <= 2e-3, e
