@@ -553,6 +553,9 @@ int sm_count() {
   return cached;
 }
 
+#ifndef PK_PREFILL_MAX_SPLIT
+#define PK_PREFILL_MAX_SPLIT 4  // key ranges per split unit at most (swept: 2..8)
+#endif
 // Tail split plan: the units of the last, partial round of the grid (one CTA
 // per SM) are cut into `split` key ranges so that round fills the SMs.
 struct SplitPlan {
@@ -568,7 +571,7 @@ SplitPlan split_plan(int B, int H, int Lq) {
   if (nsm <= 0 || p.units <= nsm) return p;
   const int rem = p.units % nsm;
   if (rem == 0) return p;
-  const int s = min(4, nsm / rem);
+  const int s = min(PK_PREFILL_MAX_SPLIT, nsm / rem);
   if (s < 2) return p;
   p.full_units = p.units - rem;
   p.split = s;
