@@ -517,20 +517,34 @@ __global__ void __launch_bounds__(256)
   const float* base = a.ws + (size_t)su * a.split * (2 * kTileM) * kPrefillPartialStride +
                       (size_t)r * kPrefillPartialStride;
   const size_t part_stride = (size_t)(2 * kTileM) * kPrefillPartialStride;
-  float M = -INFINITY;
-  for (int s = 0; s < a.split; ++s) {
-    const float* pr = base + s * part_stride;
-    if (pr[kD + 1] > 0.f) M = fmaxf(M, pr[kD]);
+  // All parts' loads issued together (split <= PK_PREFILL_MAX_SPLIT <= 8).
+  constexpr int kMaxParts = 8;
+  float ms[kMaxParts], ls[kMaxParts];
+  float4 ov[kMaxParts];
+#pragma unroll
+  for (int s = 0; s < kMaxParts; ++s) {
+    if (s < a.split) {
+      const float* pr = base + s * part_stride;
+      ms[s] = pr[kD];
+      ls[s] = pr[kD + 1];
+      ov[s] = *reinterpret_cast<const float4*>(pr + lane * 4);
+    } else {
+      ms[s] = -INFINITY;
+      ls[s] = 0.f;
+      ov[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  float M = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kMaxParts; ++s)
+    if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
   float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < a.split; ++s) {
-    const float* pr = base + s * part_stride;
-    const float ls = pr[kD + 1];
-    if (ls > 0.f) {
-      const float wgt = ex2_approx(pr[kD] - M);
-      L += ls * wgt;
-      const float4 v = *reinterpret_cast<const float4*>(pr + lane * 4);
-      o[0] += wgt * v.x; o[1] += wgt * v.y; o[2] += wgt * v.z; o[3] += wgt * v.w;
+#pragma unroll
+  for (int s = 0; s < kMaxParts; ++s) {
+    if (ls[s] > 0.f) {  // an empty part's o is never read as a number
+      const float wgt = ex2_approx(ms[s] - M);
+      L += ls[s] * wgt;
+      o[0] += wgt * ov[s].x; o[1] += wgt * ov[s].y; o[2] += wgt * ov[s].z; o[3] += wgt * ov[s].w;
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -556,6 +570,7 @@ int sm_count() {
 #ifndef PK_PREFILL_MAX_SPLIT
 #define PK_PREFILL_MAX_SPLIT 4  // key ranges per split unit at most (swept: 2..8)
 #endif
+static_assert(PK_PREFILL_MAX_SPLIT >= 1 && PK_PREFILL_MAX_SPLIT <= 8, "combine merges <= 8 parts");
 // Tail split plan: the units of the last, partial round of the grid (one CTA
 // per SM) are cut into `split` key ranges so that round fills the SMs.
 struct SplitPlan {
