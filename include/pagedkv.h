@@ -166,6 +166,42 @@ pa_status pa_decode_shared_prefix(const pa_half *q, const pa_half *k_cache,
                                   pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Groups for pa_decode_shared_prefix, derived from the block tables (host).
+ *
+ * Sequences share logical block i when their tables hold the same physical
+ * id at position i and at every earlier position (study notes "4.
+ * PagedAttention 带来的核心红利": forked sequences map their common prompt
+ * to the same blocks).  A prefix tree over each sequence's full blocks
+ * (floor(min(context_lens[b], max_blocks_per_seq*block_size) / block_size)
+ * leading entries, stopping at the first negative id) groups the sequences:
+ * where the sequences below a node part ways, at depth d blocks, they form
+ * one group sharing d*block_size tokens; a node holding more than
+ * max_group_size sequences first groups those of its children that hold two
+ * or more (they share more) and cuts the rest into groups of at most
+ * max_group_size at depth d.  No group shares fewer than min_shared_tokens
+ * (pass partition_tokens: shorter prefixes hold no whole shared partition).
+ * Each group has >= 2 members in increasing index order, groups in increasing
+ * order of their first member; the shared prefix is the exact longest common
+ * prefix of the members' full blocks.
+ *
+ * All pointers are HOST memory, row-major [B, max_blocks_per_seq] tables.
+ * Outputs, caller-allocated: seq_group[B] (group of b or -1),
+ * group_offsets[B/2 + 1], group_seqs[B], group_prefix_len[B/2] (tokens), and
+ * *num_groups.  Pass them straight to pa_decode_shared_prefix after copying
+ * to the device.  Errors: PA_ERR_INVALID for a null pointer, B < 0,
+ * max_blocks_per_seq or block_size <= 0, min_shared_tokens < 0 or
+ * max_group_size < 2 (outputs untouched except *num_groups = 0).  Host code
+ * only: no CUDA call, thread-safe, O(total full blocks * log) time.
+ * ------------------------------------------------------------------------- */
+pa_status pa_shared_prefix_groups(const int32_t *block_tables,
+                                  const int32_t *context_lens, int B,
+                                  int max_blocks_per_seq, int block_size,
+                                  int min_shared_tokens, int max_group_size,
+                                  int32_t *seq_group, int32_t *group_offsets,
+                                  int32_t *group_seqs,
+                                  int32_t *group_prefix_len, int *num_groups);
+
+/* ---------------------------------------------------------------------------
  * Decode with append: cache write of the new token fused into decode.
  *
  * Each decode step appends one token per sequence (tutorial "Block管理策略": the

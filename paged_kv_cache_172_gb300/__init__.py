@@ -10,6 +10,6 @@ from ._lib import (  # noqa: F401
     PA_DEV_BAD_SLOT, PA_DEV_TIMEOUT, PA_ERR_CUDA, PA_ERR_INVALID, PA_ERR_UNSUPPORTED,
     PA_ERR_WORKSPACE, PA_OK, PagedKVError, lib, pa_block_copy, pa_decode, pa_decode_append,
     pa_decode_partition_tokens, pa_decode_shared_prefix, pa_decode_workspace_size,
-    pa_kv_cache_write, pa_kv_cache_write_fp8, pa_decode_fp8,
+    pa_shared_prefix_groups, pa_kv_cache_write, pa_kv_cache_write_fp8, pa_decode_fp8,
     pa_prefill_chunk, pa_prefill_workspace_size, status_string,
 )

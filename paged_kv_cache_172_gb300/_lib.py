@@ -25,7 +25,8 @@ EXPORTS = (
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
     "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
     "pa_decode_static",
-    "pa_decode_append", "pa_decode_shared_prefix", "pa_kv_cache_write_fp8", "pa_decode_fp8",
+    "pa_decode_append", "pa_decode_shared_prefix", "pa_shared_prefix_groups",
+    "pa_kv_cache_write_fp8", "pa_decode_fp8",
 )
 
 # Size of the fixed scratch array behind pa_decode_static (PA_DECODE_STATIC_SCRATCH_BYTES).
@@ -77,6 +78,9 @@ def _bind(lib):
                                             _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
                                             _SZ, _P, _P]
     lib.pa_decode_shared_prefix.restype = _I
+    lib.pa_shared_prefix_groups.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                            ctypes.POINTER(_I)]
+    lib.pa_shared_prefix_groups.restype = _I
     lib.pa_kv_cache_write_fp8.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
     lib.pa_kv_cache_write_fp8.restype = _I
     lib.pa_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -245,6 +249,32 @@ def pa_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, seq
         ws_len, _ptr(status), _stream(stream, q.device))
     _check(rc, "pa_decode_shared_prefix")
     return out
+
+
+def pa_shared_prefix_groups(block_tables, context_lens, block_size, min_shared_tokens=0,
+                            max_group_size=16):
+    """Groups of sequences sharing leading physical blocks, from the block
+    tables (host-side prefix tree).  Takes CPU or CUDA int32 tensors, returns
+    CPU int32 tensors (seq_group [B], group_offsets [G+1], group_seqs [n],
+    group_prefix_len [G]) in the form pa_decode_shared_prefix takes."""
+    bt = block_tables.detach().to("cpu", torch.int32).contiguous()
+    cl = context_lens.detach().to("cpu", torch.int32).contiguous()
+    if bt.dim() != 2 or cl.dim() != 1 or cl.numel() != bt.shape[0]:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq] and context_lens [B]")
+    B, M = bt.shape
+    seq_group = torch.empty(B, dtype=torch.int32)
+    offsets = torch.empty(B // 2 + 1, dtype=torch.int32)
+    seqs = torch.empty(max(B, 1), dtype=torch.int32)
+    plen = torch.empty(max(B // 2, 1), dtype=torch.int32)
+    G = _I(0)
+    rc = lib().pa_shared_prefix_groups(_ptr(bt), _ptr(cl), B, max(M, 1), int(block_size),
+                                       int(min_shared_tokens), int(max_group_size),
+                                       _ptr(seq_group), _ptr(offsets), _ptr(seqs), _ptr(plen),
+                                       ctypes.byref(G))
+    _check(rc, "pa_shared_prefix_groups")
+    G = G.value
+    offsets = offsets[:G + 1].clone()
+    return seq_group, offsets, seqs[:int(offsets[-1])].clone(), plen[:G].clone()
 
 
 def pa_kv_cache_write_fp8(k, v, slot_mapping, k_cache8, v_cache8, k_scale, v_scale, status=None,

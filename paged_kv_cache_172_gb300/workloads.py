@@ -40,7 +40,7 @@ __all__ = [
     "PagedBatch", "TinySchedule", "tiny_schedule", "llama13b_decode",
     "prefix_sharing", "prefix_sharing_layout", "SharingLayout",
     "llama13b_context_lens", "long_context", "chunked_prefill", "random_decode",
-    "sharing_groups",
+    "sharing_groups", "fork_forest_layout",
     "random_prefill", "shuffled_pool", "fill_tables",
 ]
 
@@ -322,6 +322,42 @@ def sharing_groups(lay: "SharingLayout"):
     shared = lay.prompt_len - lay.block_size
     prefix = np.full(P, shared, dtype=np.int32)
     return seq_group, offsets, seqs, prefix
+
+
+def fork_forest_layout(seed: int, B: int, block_size: int, max_blocks: int = 24,
+                       p_root: float = 0.2):
+    """Block tables of sequences forked from one another (beam search or
+    parallel sampling), no values.  Sequence 0 is a root; sequence i > 0 is a
+    new root with probability p_root, else it forks from a uniformly chosen
+    earlier sequence at a uniform point k in [0, that sequence's full
+    blocks]: it maps the parent's first k blocks and takes fresh blocks for
+    the rest of its own length, uniform in [k+1, max_blocks] blocks.  Its
+    context length ends uniformly inside its last block.  Physical ids come
+    from a shuffled pool of exactly the blocks used.  Returns (tables
+    [B, max_blocks] int32 padded with -1, context_lens [B] int32,
+    num_blocks)."""
+    rng = np.random.default_rng(seed)
+    bs = block_size
+    chains, ctx = [], []
+    nxt = 0
+    for i in range(B):
+        if i == 0 or rng.random() < p_root:
+            k, head = 0, []
+        else:
+            par = int(rng.integers(0, i))
+            k = int(rng.integers(0, ctx[par] // bs, endpoint=True))
+            head = chains[par][:k]
+        n = int(rng.integers(max(k, 1), max_blocks, endpoint=True))
+        if n == k:  # ends on the parent's blocks: take one fresh block
+            n = k + 1
+        chains.append(head + list(range(nxt, nxt + n - k)))
+        nxt += n - k
+        ctx.append((n - 1) * bs + int(rng.integers(1, bs, endpoint=True)))
+    perm = rng.permutation(nxt).astype(np.int32)
+    tables = np.full((B, max_blocks + 1), -1, dtype=np.int32)
+    for i, c in enumerate(chains):
+        tables[i, :len(c)] = perm[np.asarray(c, dtype=np.int64)]
+    return tables, np.asarray(ctx, dtype=np.int32), nxt
 
 
 def prefix_sharing(seed: int = 2, device="cpu", H: int = 40, D: int = 128,

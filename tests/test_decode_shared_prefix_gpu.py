@@ -122,3 +122,28 @@ def test_prefix_sharing_workload():
                         batch.v_cache.cpu().numpy(), lay.tables[sel], lay.context_lens[sel],
                         batch.scale)
     assert_close(out[torch.from_numpy(sel).to(DEV)], ref, what="prefix sharing, grouped")
+
+
+@pytest.mark.parametrize("seed,bs,gmax", [(11, 16, 16), (12, 32, 4), (13, 16, 2)])
+def test_groups_from_block_tables(seed, bs, gmax):
+    """Groups derived by pa_shared_prefix_groups from a forest of forked
+    sequences drive the grouped decode to the oracle's result."""
+    H, D = 4, 128
+    tables, ctx, NB = workloads.fork_forest_layout(seed, B=48, block_size=bs, max_blocks=40,
+                                                   p_root=0.1)
+    pt = 4 * bs
+    sg, off, seqs, pref = pk.pa_shared_prefix_groups(torch.from_numpy(tables),
+                                                     torch.from_numpy(ctx), bs, pt, gmax)
+    assert pref.numel() >= 3  # the forest shares prefixes worth grouping
+    gen = torch.Generator().manual_seed(seed)
+    kc = torch.randn((NB, bs, H, D), generator=gen).half()
+    vc = torch.randn((NB, bs, H, D), generator=gen).half()
+    q = torch.randn((len(ctx), H, D), generator=gen).half()
+    scale = 1.0 / np.sqrt(D)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), tables, ctx, scale)
+    groups = tuple(t.numpy() for t in (sg, off, seqs, pref))
+    status = zero_status(DEV)
+    out = run_shared(q, kc, vc, tables, ctx, groups, gmax, pt, scale, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out, ref, what=f"derived groups seed={seed} bs={bs} gmax={gmax}")
