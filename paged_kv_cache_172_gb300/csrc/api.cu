@@ -83,6 +83,26 @@ cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_map_5d(CUtensorMap* map, const void* base, const unsigned long long dims[5],
+                        const unsigned long long strides[4], const unsigned box[5],
+                        bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < 5; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i < 4) st[i] = strides[i];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void*>(base), d, st, bx,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace pk
 
 extern "C" {
@@ -403,6 +423,8 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_INVALID;
   if (!pool_ok(num_blocks, block_size, H, D)) return PA_ERR_INVALID;
+  // the prefill kernel addresses the pool by (slot, head) rows
+  if ((long long)num_blocks * block_size * H >= (1LL << 31)) return PA_ERR_INVALID;
   if ((long long)Lq > (long long)max_blocks_per_seq * block_size) return PA_ERR_INVALID;
   const size_t need = pk::prefill_workspace_bytes(B, H, Lq);
   if (workspace != nullptr && need > 0 && workspace_bytes < need) return PA_ERR_WORKSPACE;

@@ -63,6 +63,12 @@ cudaError_t make_map_3d(CUtensorMap* map, const void* base, const unsigned long 
                         bool swizzle128,
                         CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 
+// 5-D tiled tensor map over fp16 data (same conventions, strides of dims 1..4
+// in bytes, in any order).
+cudaError_t make_map_5d(CUtensorMap* map, const void* base, const unsigned long long dims[5],
+                        const unsigned long long strides[4], const unsigned box[5],
+                        bool swizzle128);
+
 // Launch the partition kernel then the combine kernel on `stream`.  When
 // a.seq_group is set, the partition grid also computes the groups' shared-
 // prefix partitions (multi-query, from maps.ksw / maps.vsw).

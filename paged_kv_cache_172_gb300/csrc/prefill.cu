@@ -12,9 +12,10 @@
 //   warps 0-3   softmax of tile A, one query row per thread (TMEM lane = row);
 //   warps 4-7   softmax of tile B;
 //   warp 8      TMA producer: Q (4 boxes of 128 rows x 64 dims, 128-byte
-//               swizzle), then per key tile one box per (block, 64-dim half)
-//               for K and for V, gathered through the block table, into a
-//               3-slot ring in first-use order K_0, K_1, V_0, K_2, V_1, ...;
+//               swizzle), then per key tile one 5-D box per block (all its
+//               tokens, both 64-dim halves) for K and for V, gathered through
+//               the block table, into a 3-slot ring in first-use order K_0,
+//               K_1, V_0, K_2, V_1, ...;
 //   warp 9      S issuer (one thread) and tensor-memory owner;
 //   warp 10     P V issuer (one thread).
 // Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
@@ -30,12 +31,18 @@
 // landed; O_X += P_X(j) V_j once P_X(j) is stored and V_j landed.  The two
 // kinds come from two threads, so a P V product that gates a softmax never
 // queues behind S products at the issuing end.
-// Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle):
-//   Q, P, K_j   : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
-//                 the two 64-element halves 16 KB apart; the 16-byte chunk c
-//                 of row r sits at chunk position c ^ (r mod 8);
-//   V_j         : MN-major (dims contiguous): 8-key atoms 1024 B apart along
-//                 K, the two 64-dim halves 16 KB apart along N.
+// Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle; the
+// 16-byte chunk c of a 128-byte row r sits at chunk position c ^ (r mod 8)):
+//   Q, P        : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
+//                 the two 64-element halves 16 KB apart;
+//   K_j, V_j    : key groups of 8 keys x 128 dims, 2 KB apart, each holding
+//                 the 1 KB atom of dims 0-63 then that of dims 64-127 (the
+//                 order one box of a block lands in).  K_j is read K-major
+//                 (8-key atoms 2 KB apart along N, halves 1 KB apart along
+//                 K), V_j MN-major (8-key atoms 2 KB apart along K, halves
+//                 1 KB apart along N).  Fewer, larger boxes: the TMA unit
+//                 spends a fixed ~50 cycles per box besides ~2 per 128-byte
+//                 row, which bounded the K/V stream at block size 16.
 #include "pk_common.cuh"
 #include "pk_internal.h"
 #include "pk_tcgen05.cuh"
@@ -50,6 +57,7 @@ constexpr int kTileN = 128;                  // keys per tile
 constexpr int kD = 128;                      // head dim
 constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
 constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
+constexpr int kGroupBytes = 2048;            // K/V tiles: 8 keys x 128 dims
 constexpr int kStages = 3;                   // K/V ring, tiles in first-use order
 constexpr int kThreads = 352;                // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kWarpProducer = 8;
@@ -74,14 +82,17 @@ constexpr uint32_t kIdescO = tc::idesc_f16_f32(kTileM, kD, false, true);
 constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
 
 // Descriptor address offset of K step kk (16 elements = 32 B) of a K-major
-// tile: inside the 64-element half kk / 4.
+// Q or P tile: inside the 64-element half kk / 4.
 __device__ __forceinline__ constexpr uint32_t kmajor_off(int kk) {
   return (uint32_t)((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
 }
-// ... of an MN-major V tile: keys 16*kk .. 16*kk+15 are two 8-key atoms
-// starting 2048 B * kk into the tile.
+// ... of a K tile (key groups): the half's atom sits 1 KB into each group.
+__device__ __forceinline__ constexpr uint32_t kgroup_off(int kk) {
+  return (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+}
+// ... of an MN-major V tile: keys 16*kk .. 16*kk+15 are two key groups.
 __device__ __forceinline__ constexpr uint32_t vmn_off(int kk) {
-  return (uint32_t)(kk * 2048) >> 4;
+  return (uint32_t)(kk * 2 * kGroupBytes) >> 4;
 }
 
 // Ring load index of K_t and V_t (loads go K_0, then K_{t+1}, V_t per t).
@@ -234,12 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
       }
       ok = __shfl_sync(kFull, ok, 0);
-      // One box per lane (block lane / 2, 64-dim half lane % 2): a single
-      // thread would spend about 100 cycles per box issuing them in turn.
-      if (ok && lane < 2 * BPT) {
-        const int i = lane >> 1, hf = lane & 1;
-        uint8_t* dst = sKV + st * kTileBytes + hf * kSlabBytes + i * BS * 128;
-        tma_load_3d(dst, v ? &vmap : &kmap, hf * 64, h, tbl_s[lb0 - win + i] * BS, &kv_full[st]);
+      // One box per lane and block: (64 dims, 8 keys, 2 halves, BS/8 key
+      // groups) at row phys*BS*H + h of the pool seen as [slot*H + head] rows;
+      // past-the-sequence blocks (phys = num_blocks) fall outside the map and
+      // read as zeros.
+      if (ok && lane < BPT) {
+        uint8_t* dst = sKV + st * kTileBytes + lane * (BS / 8) * kGroupBytes;
+        tma_load_5d(dst, v ? &vmap : &kmap, 0, 0, 0, 0, tbl_s[lb0 - win + lane] * BS * a.H + h,
+                    &kv_full[st]);
       }
       if (ok && lane == 0) ++issued;
     };
@@ -262,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Base descriptors; each MMA adds a compile-time offset (a slot, a
         // tile or a K step never carries out of the 14-bit address field).
         const uint64_t dq = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128B);
-        const uint64_t dk = tc::smem_desc(smem_u32(sKV), 16, 1024, tc::kSwizzle128B);
+        const uint64_t dk = tc::smem_desc(smem_u32(sKV), 16, kGroupBytes, tc::kSwizzle128B);
         ok = mbar_wait(q_full, 0);
         for (int t = 0; t < n_kv && ok; ++t) {
           const int u = load_k(t);
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t db = dk + (u % kStages) * kTileDesc;
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              tc::mma_f16(tmem + x * kTileN, da + kmajor_off(kk), db + kmajor_off(kk), kIdescS,
+              tc::mma_f16(tmem + x * kTileN, da + kmajor_off(kk), db + kgroup_off(kk), kIdescS,
                           kk > 0);
             tc::commit(&s_full[x]);
           }
@@ -284,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       const uint64_t dp = tc::smem_desc(smem_u32(sP), 16, 1024, tc::kSwizzle128B);
-      const uint64_t dv = tc::smem_desc(smem_u32(sKV), kSlabBytes, 1024, tc::kSwizzle128B);
+      const uint64_t dv = tc::smem_desc(smem_u32(sKV), 1024, kGroupBytes, tc::kSwizzle128B);
       // Rows of the last key tile at or past the context length come from the
       // unused tail of the last block (never written: possibly NaN) and would
       // give P * V = 0 * NaN; the whole warp zeroes them once V has landed.
@@ -318,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* vt = sKV + (u % kStages) * kTileBytes;
             for (int i = lane; i < (kTileN - tail_rows) * 16; i += 32) {  // 16 chunks per row
               const int r = tail_rows + (i >> 4), c = i & 15;
-              *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + r * 128 + (c & 7) * 16) =
+              *reinterpret_cast<uint4*>(vt + (r >> 3) * kGroupBytes + (c >> 3) * 1024 +
+                                        (r & 7) * 128 + (c & 7) * 16) =
                   make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();  // read by the tensor core (async proxy)
@@ -620,14 +634,16 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
     if (e != cudaSuccess) return e;
   }
   {
-    unsigned long long dims[3] = {(unsigned long long)kD, (unsigned long long)a.H,
-                                  (unsigned long long)rows};
-    unsigned long long strides[2] = {(unsigned long long)kD * 2,
-                                     (unsigned long long)a.H * kD * 2};
-    unsigned box[3] = {64, 1, (unsigned)BS};
-    e = make_map_3d(&kmap, k_cache, dims, strides, box, true);
+    // The pool as rows r = slot * H + head of 128 fp16, and inside a block
+    // (rows r, r + H, ..., r + (BS-1) H from its first slot) the box order
+    // (64 dims, 8 keys, 2 halves, BS/8 key groups).
+    const unsigned long long row = (unsigned long long)kD * 2, tok = row * a.H;
+    unsigned long long dims[5] = {64, 8, 2, BS / 8, (unsigned long long)rows * a.H};
+    unsigned long long strides[4] = {tok, 128, 8 * tok, row};
+    unsigned box[5] = {64, 8, 2, BS / 8, 1};
+    e = make_map_5d(&kmap, k_cache, dims, strides, box, true);
     if (e != cudaSuccess) return e;
-    e = make_map_3d(&vmap, v_cache, dims, strides, box, true);
+    e = make_map_5d(&vmap, v_cache, dims, strides, box, true);
     if (e != cudaSuccess) return e;
   }
   auto kern = prefill_kernel<BS>;
