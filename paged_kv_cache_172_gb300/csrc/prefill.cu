@@ -18,23 +18,29 @@
 //               K_1, V_0, K_2, V_1, ...;
 //   warp 9      S issuer (one thread) and tensor-memory owner;
 //   warp 10     P V issuer (one thread).
-// Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Tensor memory: S [0,128) shared by the two tiles, Q_A [128,192) and
+// Q_B [192,256) (fp16 pairs), O_A [256,384), O_B [384,512).  Q sits in tensor
+// memory (S = Q K^T takes its A operand from there) so that shared memory
+// holds a 5-slot K/V ring: with Q in shared memory only 3 slots fit and K/V
+// tiles landed late.  Q arrives by TMA in the P buffers, which are free until
+// the first P store; each softmax thread moves its row into tensor memory.
 // Softmax of tile X, key tile j: wait for S_X(j), load the whole row into
-// registers and release S_X at once, so the tensor core computes S_X(j+1)
-// while this softmax still works on j.  Row max (keys past the row's position
+// registers and release S at once, so the tensor core computes the other
+// tile's S while this softmax still works on j.  Row max (keys past the row's position
 // skipped on diagonal tiles); p = 2^(s*scale*log2e - m) (one FMA, one ex2)
 // packed to fp16 in registers with the row sum; then wait for P_X(j-1) V_{j-1}
 // (so O_X is stable and the P_X tile free), rescale O_X only when the row max
 // grew by more than 2^8 (P then stays <= 256, exact in fp16 range), store P_X
 // to shared memory.
-// S_X(j+1) is issued once the softmax of X released S_X(j) and K_{j+1}
-// landed; O_X += P_X(j) V_j once P_X(j) is stored and V_j landed.  The two
+// The S products go A(0), B(0), A(1), B(1), ..., each once the softmax
+// released the previous one and its K tile landed; O_X += P_X(j) V_j once
+// P_X(j) is stored and V_j landed.  The two
 // kinds come from two threads, so a P V product that gates a softmax never
 // queues behind S products at the issuing end.
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle; the
 // 16-byte chunk c of a 128-byte row r sits at chunk position c ^ (r mod 8)):
-//   Q, P        : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B apart,
-//                 the two 64-element halves 16 KB apart;
+//   Q (staged), P: K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B
+//                 apart, the two 64-element halves 16 KB apart;
 //   K_j, V_j    : key groups of 8 keys x 128 dims, 2 KB apart, each holding
 //                 the 1 KB atom of dims 0-63 then that of dims 64-127 (the
 //                 order one box of a block lands in).  K_j is read K-major
@@ -58,20 +64,21 @@ constexpr int kD = 128;                      // head dim
 constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
 constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
 constexpr int kGroupBytes = 2048;            // K/V tiles: 8 keys x 128 dims
-constexpr int kStages = 3;                   // K/V ring, tiles in first-use order
+constexpr int kStages = 5;                   // K/V ring, tiles in first-use order
 constexpr int kThreads = 352;                // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                  // S = Q K^T issuer, tensor-memory owner
 constexpr int kWarpPv = 10;                  // O += P V issuer
 constexpr int kTblWindow = 256;              // block-table entries staged in smem
 constexpr int kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColQ = 128;              // Q_A, then Q_B 64 columns later
 constexpr uint32_t kColO = 256;
 
-constexpr int kOffQ = 0;                                // Q_A, Q_B
-constexpr int kOffP = kOffQ + 2 * kTileBytes;           // P_A, P_B
+constexpr int kOffP = 0;                                // P_A, P_B (Q staged first)
 constexpr int kOffKV = kOffP + 2 * kTileBytes;
 constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2;
 constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
 constexpr int kOffTbl = (kOffTmemHolder + 4 + 15) / 16 * 16;
 constexpr int kSmemBytes = kOffTbl + kTblWindow * 4 + 1024;  // + alignment slack
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
-  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sQ = smem + kOffP;  // staging only
   uint8_t* sP = smem + kOffP;
   uint8_t* sKV = smem + kOffKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -117,10 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
   uint64_t* s_full = kv_empty + kStages;  // [2] per Q tile: S_X(j) computed
-  uint64_t* s_free = s_full + 2;          // [2]: softmax holds S_X(j) in registers
+  uint64_t* s_free = s_full + 2;          // [2]: softmax of X holds S in registers
   uint64_t* p_full = s_free + 2;          // [2]: P_X(j) stored
   uint64_t* pv_done = p_full + 2;         // [2]: O_X += P_X(j) V_j completed
   uint64_t* drain = pv_done + 2;
+  uint64_t* q_ready = drain + 1;          // [2]: Q_X moved into tensor memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
   int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
 
@@ -186,9 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], 4);  // one arrival per softmax warp
+      mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&q_ready[i], 4);
     }
     mbar_init(drain, 2);
     fence_mbar_init();
@@ -274,23 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // Base descriptors; each MMA adds a compile-time offset (a slot, a
         // tile or a K step never carries out of the 14-bit address field).
-        const uint64_t dq = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128B);
         const uint64_t dk = tc::smem_desc(smem_u32(sKV), 16, kGroupBytes, tc::kSwizzle128B);
-        ok = mbar_wait(q_full, 0);
+        int last_x = -1, last_t = 0;  // the S product issued last
         for (int t = 0; t < n_kv && ok; ++t) {
           const int u = load_k(t);
           for (int x = 0; x < 2 && ok; ++x) {
             if (t >= nt[x]) continue;
-            if (t > 0 && !(ok = mbar_wait(&s_free[x], (t - 1) & 1))) break;
+            if (t == 0 && !(ok = mbar_wait(&q_ready[x], 0))) break;
+            // S is free once the softmax of the previous product loaded it
+            if (last_x >= 0 && !(ok = mbar_wait(&s_free[last_x], last_t & 1))) break;
             if (!(ok = landed(u))) break;
             tc::fence_after_sync();
-            const uint64_t da = dq + x * kTileDesc;
             const uint64_t db = dk + (u % kStages) * kTileDesc;
+            const uint32_t ta = tmem + kColQ + x * (kD / 2);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              tc::mma_f16(tmem + x * kTileN, da + kmajor_off(kk), db + kgroup_off(kk), kIdescS,
-                          kk > 0);
+              tc::mma_f16_ts(tmem + kColS, ta + kk * 8, db + kgroup_off(kk), kIdescS, kk > 0);
             tc::commit(&s_full[x]);
+            last_x = x;
+            last_t = t;
           }
           if (ok) tc::commit(&kv_empty[u % kStages]);  // K_t has no further reader
         }
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_s = tmem + t_lane + x * kTileN;
+    const uint32_t t_s = tmem + t_lane + kColS;
     const uint32_t t_o = tmem + t_lane + kColO + x * kD;
     const int pos0 = x ? pos0_b : pos0_a;
     const int pos = pos0 + row;
@@ -358,6 +369,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     uint8_t* prow = sP + x * kTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
+    // Q row (staged by TMA in the P tile, 128-byte swizzle) into tensor
+    // memory: column c of Q_X holds dims 2c, 2c+1.
+    ok = __all_sync(kFull, mbar_wait(q_full, 0));
+    if (ok) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(prow + hf * kSlabBytes +
+                                                          ((c ^ (row & 7)) * 16));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tc::st_32x32(tmem + t_lane + kColQ + x * (kD / 2) + hf * 32, w);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[x]);
+    }
     for (int j = 0; j < ntile && ok; ++j) {
       if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
@@ -369,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) tc::ld_32x32(t_s + c * 32, r[c]);
       tc::wait_ld();
       tc::fence_before_sync();
-      mbar_arrive(&s_free[x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[x]);  // one arrival per warp
       if (diag) {  // keys past this row's position: -inf
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -383,9 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[c][i]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        for (int i = 0; i < 32; i += 2)
+          mx[(i >> 1) & 7] = max3f(mx[(i >> 1) & 7], __uint_as_float(r[c][i]),
+                                   __uint_as_float(r[c][i + 1]));
+      const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7])) * sl2;
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + 8.0f;
       float alpha = 1.f;
@@ -397,19 +434,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P = 2^(s * scale * log2e - m) packed to fp16 pairs in place (the
       // first 16 words of each 32-key chunk), row sum.  A masked key has
       // s = -inf, so p = 0.
+      // Packed pairs: one FMA and one add instruction per two keys.
       const float neg_m = -m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), sl2, neg_m));
-          rs[e & 3] += p0 + p1;
+          float y0, y1;
+          fma_f32x2(y0, y1, __uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]), sl2,
+                    sl2, neg_m, neg_m);
+          const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          const int k = 2 * (e & 3);
+          add_f32x2(rs[k], rs[k + 1], rs[k], rs[k + 1], p0, p1);
           __half2 hp = __floats2half2_rn(p0, p1);
           r[c][e] = *reinterpret_cast<uint32_t*>(&hp);
         }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       // P_X(j-1) V_{j-1} done: the P_X tile is free, O_X is stable.
       if (j > 0) {
         if (!(ok = __all_sync(kFull, mbar_wait(&pv_done[x], (j - 1) & 1)))) break;
@@ -440,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
       tc::fence_before_sync();
-      mbar_arrive(&p_full[x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[x]);
     }
     if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&pv_done[x], (ntile - 1) & 1));
     if (ok && part >= 0) {
