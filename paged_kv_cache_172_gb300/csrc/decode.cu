@@ -194,12 +194,23 @@ struct PartitionCfg {
   static constexpr int RL = FP8 ? 16 : 32;
   static constexpr int NT = 32 / RL;                  // tokens per warp instruction
   static constexpr int EPL = D / RL;                  // dims per lane
-  static constexpr int TB = BS < 16 ? BS : 16;        // tokens per TMA box / pipeline stage
-  static constexpr int SUB = BS / TB;                 // stages per physical block
+  // Tokens per pipeline stage: 16 fp16 rows (4 KB per head at D = 128), or 32
+  // e4m3 rows at block size >= 16 -- the same bytes per stage, and every lane
+  // then holds a distinct token's score, so the per-stage reductions cost half
+  // as much per token.  A TMA box never spans blocks: TBX tokens, BPS per stage.
+  static constexpr int TB = FP8 ? (BS >= 16 ? 32 : BS) : (BS < 16 ? BS : 16);
+  static constexpr int TBX = TB < BS ? TB : BS;       // tokens per TMA box
+  static constexpr int BPS = TB / TBX;                // boxes per tensor per stage
+  static constexpr int SUB = BS / TBX;                // boxes per physical block
   static constexpr int ELEM = FP8 ? 1 : 2;            // bytes per stored K/V element
   static constexpr int TILE_BYTES = TB * D * ELEM;    // one head's rows of one stage
   static constexpr int SCALE_BYTES = FP8 ? TB * 4 : 0;  // per-token scales of one stage
-  static constexpr int SCALE_SLOT = FP8 ? 128 : 0;      // 128-byte aligned TMA destination
+  // Scales of one tensor and stage: box k of TBX tokens at byte k * 128 (a TMA
+  // destination in shared memory must be 128-byte aligned).
+  static constexpr int SCALE_SLOT = FP8 ? BPS * 128 : 0;
+  static_assert(!FP8 || TBX * 4 <= 128, "one box of scales per 128-byte slot");
+  // Float index of token t's scale inside a scale slot.
+  static __device__ __forceinline__ int scale_index(int t) { return (t / TBX) * 32 + t % TBX; }
   // stage = [K rows][V rows][K scales][V scales]; TX_BYTES actually land
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SCALE_SLOT;
   static constexpr int TX_BYTES = 2 * TILE_BYTES + 2 * SCALE_BYTES;
@@ -299,19 +310,25 @@ __global__ void __launch_bounds__(WARPS * 32)
   __syncwarp();
 
   // Prologue: fill the pipeline.  Unit u is tokens [u*TB, u*TB+TB) of the
-  // partition: sub-block u % SUB of logical block lb0 + u / SUB.
+  // partition; its box k holds tokens u*TB + k*TBX + [0, TBX), inside logical
+  // block lb0 + (u*TB + k*TBX) / BS.
   auto issue = [&](int u, int s) {  // all lanes (shuffle), lane 0 issues
-    const int pb = __shfl_sync(kFull, phys, u / SUB);
-    if (lane == 0) {
-      uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
-      const int row = pb * BS + (u % SUB) * TB;
-      mbar_arrive_expect_tx(&bars[s], Cfg::TX_BYTES);
-      tma_load_3d(st, &maps.k, 0, h, row, &bars[s]);
-      tma_load_3d(st + Cfg::TILE_BYTES, &maps.v, 0, h, row, &bars[s]);
-      if constexpr (FP8) {  // scales [num_blocks, H, bs]: box of TB tokens
-        tma_load_3d(st + 2 * Cfg::TILE_BYTES, &maps.ks, (u % SUB) * TB, h, pb, &bars[s]);
-        tma_load_3d(st + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT, &maps.vs, (u % SUB) * TB, h, pb,
+    uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[s], Cfg::TX_BYTES);
+#pragma unroll
+    for (int k = 0; k < Cfg::BPS; ++k) {
+      const int tt = u * TB + k * Cfg::TBX;  // first token of the box in the partition
+      const int pb = __shfl_sync(kFull, phys, tt / BS);
+      if (lane == 0) {
+        const int row = pb * BS + tt % BS;
+        tma_load_3d(st + k * Cfg::TBX * D * Cfg::ELEM, &maps.k, 0, h, row, &bars[s]);
+        tma_load_3d(st + Cfg::TILE_BYTES + k * Cfg::TBX * D * Cfg::ELEM, &maps.v, 0, h, row,
                     &bars[s]);
+        if constexpr (FP8) {  // scales [num_blocks, H, bs]: box of TBX tokens
+          tma_load_3d(st + 2 * Cfg::TILE_BYTES + k * 128, &maps.ks, tt % BS, h, pb, &bars[s]);
+          tma_load_3d(st + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT + k * 128, &maps.vs, tt % BS, h,
+                      pb, &bars[s]);
+        }
       }
     }
   };
@@ -396,7 +413,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
 
     float dot = part_dot[0];
-    if constexpr (FP8) dot *= kscl[my_tok];  // per-(token, head) dequantization scale
+    if constexpr (FP8) dot *= kscl[Cfg::scale_index(my_tok)];  // per-(token, head) scale
     float sc = (my_tok < valid) ? dot * a.scale_log2 : -INFINITY;
     float mb = sc;
 #pragma unroll
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     // its weight; instruction it broadcasts the weights of its NT tokens.
     float wv = pr;
     if constexpr (FP8) wv = __uint_as_float((uint32_t)__half_as_ushort(
-                           __float2half_rn(pr * 256.f * vscl[my_tok])));
+                           __float2half_rn(pr * 256.f * vscl[Cfg::scale_index(my_tok)])));
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
       const int t = it * NT + lane / RL;
@@ -575,7 +592,7 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
 #endif
 
 #ifndef PK_DECODE_FP8_NSTAGE
-#define PK_DECODE_FP8_NSTAGE 3
+#define PK_DECODE_FP8_NSTAGE 2
 #endif
 
 template <int D, int BS, bool FP8>
@@ -588,8 +605,14 @@ struct DecodeTuning {
   static constexpr int RAW = PK_DECODE_INFLIGHT_BYTES / STAGE;
   static constexpr int NSTAGE16 = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
 #endif
-  // e4m3 stages hold half the bytes: more of them keep as much in flight
-  static constexpr int NSTAGE = FP8 ? PK_DECODE_FP8_NSTAGE : NSTAGE16;
+  // e4m3 stages of 32 tokens hold as many bytes as 16 fp16 tokens: two per
+  // warp, as for fp16, keeps three CTAs per SM (three stages leave two).
+  // Below block size 16 a stage is one block: enough of them for the bytes.
+  static constexpr int STAGE8 = 2 * BS * D;
+  static constexpr int RAW8 = PK_DECODE_INFLIGHT_BYTES / STAGE8;
+  static constexpr int NSTAGE = !FP8 ? NSTAGE16
+                                     : (BS >= 16 ? PK_DECODE_FP8_NSTAGE
+                                                 : (RAW8 < 2 ? 2 : (RAW8 > 8 ? 8 : RAW8)));
 };
 
 // Programmatic stream serialisation: the kernel may be scheduled before its
