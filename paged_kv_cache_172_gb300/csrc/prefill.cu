@@ -80,7 +80,8 @@ constexpr int kOffKV = kOffP + 2 * kTileBytes;
 constexpr int kOffBar = kOffKV + kStages * kTileBytes;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2;
 constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
-constexpr int kOffTbl = (kOffTmemHolder + 4 + 15) / 16 * 16;
+constexpr int kOffIssued = kOffTmemHolder + 4;          // [2] S products issued per tile
+constexpr int kOffTbl = (kOffIssued + 8 + 15) / 16 * 16;
 constexpr int kSmemBytes = kOffTbl + kTblWindow * 4 + 1024;  // + alignment slack
 
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -100,6 +101,18 @@ __device__ __forceinline__ constexpr uint32_t kgroup_off(int kk) {
 // ... of an MN-major V tile: keys 16*kk .. 16*kk+15 are two key groups.
 __device__ __forceinline__ constexpr uint32_t vmn_off(int kk) {
   return (uint32_t)(kk * 2 * kGroupBytes) >> 4;
+}
+
+// Wait until the S issuer has issued `n` S products of a tile (its counter
+// only grows); false after kWaitLimitCycles.
+__device__ __forceinline__ bool wait_issued(volatile int* cnt, int n) {
+  if (*cnt >= n) return true;
+  const long long t0 = clock64();
+  while (*cnt < n) {
+    __nanosleep(32);
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
 }
 
 // Ring load index of K_t and V_t (loads go K_0, then K_{t+1}, V_t per t).
@@ -131,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_ready = drain + 1;          // [2]: Q_X moved into tensor memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
   int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
+  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -187,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblk_seq = (n + BS - 1) / BS;
 
   if (threadIdx.x == 0) {
+    s_issued[0] = 0;
+    s_issued[1] = 0;
     mbar_init(q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -300,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kD / 16; ++kk)
               tc::mma_f16_ts(tmem + kColS, ta + kk * 8, db + kgroup_off(kk), kIdescS, kk > 0);
             tc::commit(&s_full[x]);
+            s_issued[x] = t + 1;  // read by the P V issuer (a scheduling hint only)
             last_x = x;
             last_t = t;
           }
@@ -319,6 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t >= nt[x]) continue;
           if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
           if (!(ok = landed(u))) break;
+          // Keep the tensor core's queue in chain order: P_X(t) V_t goes in
+          // behind S_X(t+1), so that S product never waits for it.  The S
+          // chain does not depend on this product, so the wait ends.
+          if (t + 1 < nt[x] && !(ok = wait_issued(s_issued + x, t + 2))) break;
           tc::fence_after_sync();
           const uint64_t da = dp + x * kTileDesc;
           const uint64_t db = dv + (u % kStages) * kTileDesc;
