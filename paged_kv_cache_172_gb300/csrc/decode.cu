@@ -291,17 +291,6 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   // Dims [dl, dl + EPL) of this lane; lane / RL picks the token of a pair.
   const int dl = (lane % RL) * EPL;
-  // Query slice of this lane (and, for e4m3 pools, its fp16 pairs).
-  float qf[EPL];
-  uint32_t qh[EPL / 2];
-  {
-    LaneVec<EPL> qv;
-    qv.load(a.q + row_bh * D + dl);
-    qv.to_float(qf);
-#pragma unroll
-    for (int e = 0; e < EPL / 2; ++e)
-      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + dl)[e];
-  }
 
   if (lane == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
@@ -333,6 +322,19 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   };
   for (int i = 0; i < NSTAGE && i < nunit; ++i) issue(i, i);
+
+  // Query slice of this lane (and, for e4m3 pools, its fp16 pairs), read once
+  // the first stages are in flight so that its latency overlaps the K/V copies.
+  float qf[EPL];
+  uint32_t qh[EPL / 2];
+  {
+    LaneVec<EPL> qv;
+    qv.load(a.q + row_bh * D + dl);
+    qv.to_float(qf);
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e)
+      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + dl)[e];
+  }
 
   float m = -INFINITY, l = 0.f;
   float o[EPL];
@@ -511,6 +513,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 // the partition count so a 1M-token context (thousands of partitions) still
 // keeps many loads in flight; W == 1 for short contexts needs no CTA sync.
 constexpr int kMaxCombineWarps = 16;
+constexpr int kFastParts = 16;  // combine: parts merged from registers by one warp
 
 template <int D>
 __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const DecodeArgs a) {
@@ -518,13 +521,61 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
   pdl_wait();  // partitions come from the partition kernel just before
   const int b = blockIdx.x;
   const int h = blockIdx.y;
-  const int ctx = checked_ctx(a, b, false);
-  const int n = (ctx + a.part_tokens - 1) / a.part_tokens;
-  if (n <= 1) return;
   const int W = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row0 = ((size_t)b * a.H + h) * a.num_parts;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row0;
+  if (W == 1 && a.num_parts <= kFastParts) {
+    // One warp, few parts: every part's (m, l) and output slice are loaded
+    // at once (slots past n hold stale data and are masked), so the merge
+    // waits on one round trip to L2 instead of two.
+    float2 mlv = make_float2(-INFINITY, 0.f);
+    if (lane < a.num_parts) mlv = ml[lane];
+    float ov[kFastParts][EPL];
+#pragma unroll
+    for (int s = 0; s < kFastParts; ++s) {
+      if (s < a.num_parts) {
+        const float* src = a.ws_o + (row0 + s) * D + lane * EPL;
+        if constexpr (EPL == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(src);
+          ov[s][0] = t.x; ov[s][1] = t.y; ov[s][2] = t.z; ov[s][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(src);
+          ov[s][0] = t.x; ov[s][1] = t.y;
+        }
+      }
+    }
+    const int n = (checked_ctx(a, b, false) + a.part_tokens - 1) / a.part_tokens;
+    if (n <= 1) return;  // the partition kernel wrote the row itself
+    if (lane >= n) mlv = make_float2(-INFINITY, 0.f);
+    float mx = mlv.x;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float wl = lane < n ? fast_exp2(mlv.x - mx) : 0.f;  // weight of part `lane`
+    float lsum = wl * mlv.y;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kFastParts; ++s) {
+      const float w = __shfl_sync(kFull, wl, s);
+      if (s < n) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, ov[s][e], acc[e]);
+      }
+    }
+    const float inv = 1.f / lsum;
+    float r[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) r[e] = acc[e] * inv;
+    store_half_row<EPL>(a.out + ((size_t)b * a.H + h) * D + lane * EPL, r);
+    return;
+  }
+  const int ctx = checked_ctx(a, b, false);
+  const int n = (ctx + a.part_tokens - 1) / a.part_tokens;
+  if (n <= 1) return;
 
   __shared__ float red_m[kMaxCombineWarps];
   __shared__ float red_l[kMaxCombineWarps];
