@@ -123,7 +123,8 @@ template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
   constexpr int BPT = kTileN / BS;  // blocks per key tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -386,7 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos0 = x ? pos0_b : pos0_a;
     const int pos = pos0 + row;
     const int ntile = x ? ntile_b : ntile_a;
-    const int rows = x ? rows_b : rows_a;
     const float sl2 = a.scale_log2;
     uint8_t* prow = sP + x * kTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
@@ -530,11 +530,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wrow[kD] = ntile > 0 ? m : -INFINITY;
       wrow[kD + 1] = ntile > 0 ? l : 0.f;
     } else if (ok && ntile > 0) {
+      // The output tile goes through the P tile (free: every P V product of X
+      // is done), swizzled like the TMA tiles, and leaves by two TMA stores:
+      // one 16 KB copy per 64-dim half instead of 16 scattered 16-byte stores
+      // per thread.  Rows past the chunk fall outside the tensor map and are
+      // not written.
       tc::fence_after_sync();
       const float inv = 1.f / l;
-      __half* orow = a.out + (out_row0 + x * kTileM + row) * kD;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {  // dims 32c .. 32c+31
         uint32_t o[32];
         tc::ld_32x32(t_o + c * 32, o);
         tc::wait_ld();
@@ -545,12 +549,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         __uint_as_float(o[2 * i + 1]) * inv);
           hv[i] = *reinterpret_cast<uint32_t*>(&t);
         }
-        if (row < rows) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        uint8_t* slab = prow + (c >> 1) * kSlabBytes;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = (((c & 1) << 2) + q) ^ (row & 7);
+          *reinterpret_cast<uint4*>(slab + chunk * 16) =
+              make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
         }
+      }
+      fence_proxy_async_smem();  // read by the TMA unit (async proxy)
+      named_bar_sync(1 + x, 128);
+      if (quarter == 0 && lane == 0) {
+        const int bh = b * a.H + h;
+        tma_store_3d(&omap, sP + x * kTileBytes, 0, q0 + x * kTileM, bh);
+        tma_store_3d(&omap, sP + x * kTileBytes + kSlabBytes, 64, q0 + x * kTileM, bh);
+        bulk_commit_group();
+        bulk_wait_all();  // the shared-memory source stays valid until the CTA exits
       }
     }
   }
@@ -684,7 +698,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
   }
   a.full_units = plan.full_units;
   a.split = plan.split;
-  CUtensorMap qmap, kmap, vmap;
+  CUtensorMap qmap, kmap, vmap, omap;
   const long long rows = (long long)a.num_blocks * BS;
   cudaError_t e;
   {
@@ -694,6 +708,8 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
                                      (unsigned long long)a.Lq * kD * 2};
     unsigned box[3] = {64, kTileM, 1};
     e = make_map_3d(&qmap, a.q, dims, strides, box, true);
+    if (e != cudaSuccess) return e;
+    e = make_map_3d(&omap, a.out, dims, strides, box, true);  // same layout as q
     if (e != cudaSuccess) return e;
   }
   {
@@ -726,7 +742,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
+  e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, omap, a);
   if (e != cudaSuccess || plan.split == 1) return e;
   const int n_split = plan.units - plan.full_units;
   cudaLaunchConfig_t cc = {};
