@@ -84,15 +84,16 @@ def test_prefill_permutation_invariance_bit_exact():
     assert torch.equal(out, out2)
 
 
-def test_prefill_value_ones_and_bad_context():
-    batch = workloads.random_prefill(2, 2, 128, 16, 130, [500, 130], seed=52, device=DEV,
+@pytest.mark.parametrize("Lq", [130, 300])  # one and two work units per (sequence, head)
+def test_prefill_value_ones_and_bad_context(Lq):
+    batch = workloads.random_prefill(2, 2, 128, 16, Lq, [Lq + 370, Lq], seed=52, device=DEV,
                                      write_chunk=False)
     g = to_dev(batch, DEV)
     out = run_prefill(dict(g, v_cache=torch.ones_like(g["v_cache"])), batch.scale)
     assert torch.all(out == 1.0)
     status = zero_status(DEV)
     bad = g["context_lens"].clone()
-    bad[1] = 129  # shorter than the chunk
+    bad[1] = Lq - 1  # shorter than the chunk
     out = torch.full_like(g["q"], 3.0)
     run_prefill(dict(g, context_lens=bad), batch.scale, status=status, out=out)
     torch.cuda.synchronize()
@@ -164,5 +165,41 @@ def test_tail_split_matches_whole_units_and_oracle():
                          sl(batch.v_cache).numpy(), batch.block_tables.numpy(),
                          batch.context_lens.numpy(), batch.scale)
     assert_close(out_split[:, hs], ref, what="tail-split heads")
+    e = errors(out_split, out_whole.float().cpu().numpy().astype(np.float64))
+    assert e[0] <= 2e-3, e
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("Lq,ctx", [(257, [257, 900]), (384, [1000, 500]), (512, [512, 1200]),
+                                    (640, [700, 1500]), (1000, [1100, 1000])])
+def test_prefill_long_chunks_ragged(bs, Lq, ctx):
+    """Chunks of several 256-query work units per (sequence, head), the last one
+    ragged inside either of its two Q tiles."""
+    check_against_oracle(len(ctx), 2, bs, Lq, ctx, seed=60 + Lq + bs,
+                         what=f"long chunk bs={bs} Lq={Lq} {ctx}")
+
+
+def test_tail_split_two_units_per_head():
+    # One sequence, 512 queries: two work units per head; SMs / 2 + 6 heads
+    # leave a partial last round (12 units), split into key ranges.
+    nsm = torch.cuda.get_device_properties(DEV).multi_processor_count
+    H, Lq, bs = nsm // 2 + 6, 512, 16
+    ctx = [Lq + 3 * 128 + 77]
+    batch = workloads.random_prefill(1, H, 128, bs, Lq, ctx, seed=96, device="cpu",
+                                     write_chunk=False)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out_split = run_prefill(g, batch.scale, status=status)
+    out_whole = pk.pa_prefill_chunk(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                    g["context_lens"], batch.scale, tail_split=False,
+                                    status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    hs = list(range(H - 8, H))
+    sl = lambda t: t[:, :, hs].contiguous()
+    ref = oracle.prefill(batch.q[:, hs].contiguous().numpy(), sl(batch.k_cache).numpy(),
+                         sl(batch.v_cache).numpy(), batch.block_tables.numpy(),
+                         batch.context_lens.numpy(), batch.scale)
+    assert_close(out_split[:, hs], ref, what="tail-split heads, two units each")
     e = errors(out_split, out_whole.float().cpu().numpy().astype(np.float64))
     assert e[0] <= 2e-3, e

@@ -42,12 +42,12 @@ def poison(batch):
     return int((~used).sum()), len(tails)
 
 
+@pytest.mark.parametrize("Lq", [200, 400])  # one and two work units per (sequence, head)
 @pytest.mark.parametrize("bs", [16, 32])
-def test_prefill_ignores_stale_slots(bs):
-    Lq = 200
+def test_prefill_ignores_stale_slots(bs, Lq):
     ctx = [Lq + 333, Lq + 1007, Lq + 9]  # partial last blocks
-    batch = workloads.random_prefill(len(ctx), 3, 128, bs, Lq, ctx, seed=300 + bs, device="cpu",
-                                     write_chunk=False)
+    batch = workloads.random_prefill(len(ctx), 3, 128, bs, Lq, ctx, seed=300 + bs + Lq,
+                                     device="cpu", write_chunk=False)
     n_unused, n_tails = poison(batch)
     assert n_tails == len(ctx)
     ref = oracle.prefill(batch.q.numpy(), batch.k_cache.numpy(), batch.v_cache.numpy(),
@@ -59,7 +59,7 @@ def test_prefill_ignores_stale_slots(bs):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert torch.isfinite(out).all()
-    assert_close(out, ref, what=f"prefill with NaN in unread slots bs={bs}")
+    assert_close(out, ref, what=f"prefill with NaN in unread slots bs={bs} Lq={Lq}")
 
 
 @pytest.mark.parametrize("bs", [4, 16, 32])
