@@ -218,6 +218,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 2);
     fence_mbar_init();
+    // Q goes out first, before tensor memory is allocated and the CTA syncs:
+    // it heads the start-up path (Q -> tensor memory -> first S product).
+    const int bh = b * a.H + h;
+    mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      tma_load_3d(sQ + x * kTileBytes, &qmap, 0, q0 + x * kTileM, bh, q_full);
+      tma_load_3d(sQ + x * kTileBytes + kSlabBytes, &qmap, 64, q0 + x * kTileM, bh, q_full);
+    }
+  }
+  // The producer's first block-table window, in flight across the sync.
+  constexpr int kPerLane = kTblWindow / 32;
+  int ent0[kPerLane];
+  if (warp == kWarpProducer) {
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+      const int lb = kt0 * BPT + lane + 32 * k;
+      ent0[k] = lb < nblk_seq ? __ldg(a.block_tables + (size_t)b * a.max_blocks + lb)
+                              : a.num_blocks;
+    }
   }
   if (warp == kWarpMma) {
     tc::tmem_alloc(tmem_holder, kTmemCols);
@@ -236,13 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
-      const int bh = b * a.H + h;
-      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        tma_load_3d(sQ + x * kTileBytes, &qmap, 0, q0 + x * kTileM, bh, q_full);
-        tma_load_3d(sQ + x * kTileBytes + kSlabBytes, &qmap, 64, q0 + x * kTileM, bh, q_full);
-      }
     }
     // Key tile t (K when v == 0, else V) into ring slot u % kStages.
     auto load_tile = [&](int t, int v, int u) {
@@ -251,17 +264,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K_t is requested before V_{t-1}: start the window one tile early.
         win = (v == 0 && t > 0) ? lb0 - BPT : lb0;
         __syncwarp();
-        for (int i = lane; i < kTblWindow; i += 32) {
-          const int lb = win + i;
-          int phys = a.num_blocks;  // past the sequence: outside the map, TMA fills zeros
-          if (lb < nblk_seq) {
-            phys = a.block_tables[(size_t)b * a.max_blocks + lb];
-            if (phys < 0 || phys >= a.num_blocks) {
-              flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
-              phys = a.num_blocks;
-            }
+        // All of the window's loads in flight at once (one round trip, not
+        // one per 32 entries: this sits on the CTA's start-up path).
+        int ent[kPerLane];
+        if (win == kt0 * BPT && t == 0) {  // the first window, loaded before the sync
+#pragma unroll
+          for (int k = 0; k < kPerLane; ++k) ent[k] = ent0[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < kPerLane; ++k) {
+            const int lb = win + lane + 32 * k;
+            ent[k] = lb < nblk_seq ? __ldg(a.block_tables + (size_t)b * a.max_blocks + lb)
+                                   : a.num_blocks;  // past the sequence: TMA fills zeros
           }
-          tbl_s[i] = phys;
+        }
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          int phys = ent[k];
+          if (phys < 0 || phys > a.num_blocks ||
+              (phys == a.num_blocks && win + lane + 32 * k < nblk_seq)) {
+            flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            phys = a.num_blocks;
+          }
+          tbl_s[lane + 32 * k] = phys;
         }
         __syncwarp();
       }
