@@ -44,6 +44,9 @@ L2_FLUSH_BYTES = 512 << 20
 # 38-sequence batch, keyed by the hash of the decode source it was taken on;
 # null once the source changes.
 DECODE_TRAFFIC = {"e5400aa6b9efdd8f": 853227008 + 6305024}
+# The same for one launch of the chunked-prefill kernel (8 x 512 queries on
+# 3,584 cached tokens, block size 16), keyed by the hash of the prefill source.
+PREFILL_TRAFFIC = {("167764288f8a5ffe", 16): 713364224 + 46671872}
 
 
 def src_hash(name):
@@ -607,6 +610,9 @@ def run_aux(args, name):
                      "traffic": None},
         "clocks": clocks.summary(),
     }
+    if name == "chunked_prefill":
+        line["roofline"]["traffic"] = PREFILL_TRAFFIC.get((src_hash("prefill.cu"), args.block_size))
+        line["roofline"]["traffic_kernel"] = "prefill_kernel"
     line.update(extra)
     if name == "prefix_sharing":
         line["logical_GBs"] = logical / main_s / 1e9
