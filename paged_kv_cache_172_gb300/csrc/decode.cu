@@ -61,19 +61,6 @@ struct LaneVec<4> {
   }
 };
 template <>
-struct LaneVec<8> {
-  uint4 raw;
-  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint4*>(p); }
-  __device__ __forceinline__ void to_float(float* f) const {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      f[2 * i] = a.x; f[2 * i + 1] = a.y;
-    }
-  }
-};
-template <>
 struct LaneVec<2> {
   uint32_t raw;
   __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
@@ -96,83 +83,99 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c) {
   return d;
 }
 
-// Lane partial of q . k for EPL e4m3 codes of k (fp16 query pairs qh).
+// N consecutive 32-bit words from p (4 N bytes, aligned to min(16, 4 N)).
+template <int N>
+__device__ __forceinline__ void load_words(uint32_t* w, const void* p) {
+  if constexpr (N == 1) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    static_assert(N % 4 == 0, "whole 16-byte chunks");
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+  }
+}
+
+// Four e4m3 codes (one word) as two fp16 pairs; exact.
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2_raw l = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Lane partial of q . k for EPL e4m3 codes of k (fp16 query pairs qh); from 16
+// dims on, two interleaved sums shorten the dependent chain.
 template <int EPL>
 __device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) {
-  if constexpr (EPL == 8) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p);
-    const uint32_t w[2] = {raw.x, raw.y};
-    float t = 0.f;
+  static_assert(EPL % 4 == 0, "whole words of codes");
+  constexpr int NW = EPL / 4, NACC = EPL >= 16 ? 2 : 1;
+  uint32_t w[NW];
+  load_words<NW>(w, p);
+  float t[NACC];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-      t = fma2_f16_f32(qh[2 * i], *reinterpret_cast<const uint32_t*>(&lo), t);
-      t = fma2_f16_f32(qh[2 * i + 1], *reinterpret_cast<const uint32_t*>(&hi), t);
-    }
-    return t;
-  } else if constexpr (EPL == 4) {
-    const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
-    const float t = fma2_f16_f32(qh[0], *reinterpret_cast<const uint32_t*>(&lo), 0.f);
-    return fma2_f16_f32(qh[1], *reinterpret_cast<const uint32_t*>(&hi), t);
-  } else {
-    const uint16_t raw = *reinterpret_cast<const uint16_t*>(p);
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)raw, __NV_E4M3);
-    return fma2_f16_f32(qh[0], *reinterpret_cast<const uint32_t*>(&lo), 0.f);
+  for (int k = 0; k < NACC; ++k) t[k] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    uint32_t lo, hi;
+    e4m3x4_to_half2x2(w[i], lo, hi);
+    t[i % NACC] = fma2_f16_f32(qh[2 * i], lo, t[i % NACC]);
+    t[i % NACC] = fma2_f16_f32(qh[2 * i + 1], hi, t[i % NACC]);
   }
+  if constexpr (NACC == 2) return t[0] + t[1];
+  return t[0];
 }
 
 // o[e] += w * v[e] for EPL e4m3 codes v (exact in fp16), products exact in
 // fp32, one rounding per addition.
 template <int EPL>
 __device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint8_t* p) {
+  static_assert(EPL % 4 == 0, "whole words of codes");
+  constexpr int NW = EPL / 4;
   const uint16_t wb = __half_as_ushort(w);
-  if constexpr (EPL == 8) {
-    axpy_e4m3<4>(o, w, p);
-    axpy_e4m3<4>(o + 4, w, p + 4);
-  } else if constexpr (EPL == 4) {
-    const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw & 0xffffu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(raw >> 16), __NV_E4M3);
+  uint32_t wd[NW];
+  load_words<NW>(wd, p);
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    uint32_t lo, hi;
+    e4m3x4_to_half2x2(wd[i], lo, hi);
     asm("{\n\t.reg .f16 w, b0, b1, b2, b3;\n\tmov.b16 w, %4;\n\t"
         "mov.b32 {b0, b1}, %5;\n\tmov.b32 {b2, b3}, %6;\n\t"
         "fma.rn.f32.f16 %0, w, b0, %0;\n\tfma.rn.f32.f16 %1, w, b1, %1;\n\t"
         "fma.rn.f32.f16 %2, w, b2, %2;\n\tfma.rn.f32.f16 %3, w, b3, %3;\n\t}"
-        : "+f"(o[0]), "+f"(o[1]), "+f"(o[2]), "+f"(o[3])
-        : "h"(wb), "r"(*reinterpret_cast<const uint32_t*>(&lo)),
-          "r"(*reinterpret_cast<const uint32_t*>(&hi)));
-  } else {
-    const uint16_t raw = *reinterpret_cast<const uint16_t*>(p);
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)raw, __NV_E4M3);
-    asm("{\n\t.reg .f16 w, b0, b1;\n\tmov.b16 w, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
-        "fma.rn.f32.f16 %0, w, b0, %0;\n\tfma.rn.f32.f16 %1, w, b1, %1;\n\t}"
-        : "+f"(o[0]), "+f"(o[1])
-        : "h"(wb), "r"(*reinterpret_cast<const uint32_t*>(&lo)));
+        : "+f"(o[4 * i]), "+f"(o[4 * i + 1]), "+f"(o[4 * i + 2]), "+f"(o[4 * i + 3])
+        : "h"(wb), "r"(lo), "r"(hi));
   }
+}
+
+// Warp maximum of a float (NaN-free inputs; -inf allowed), one instruction.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 template <int EPL>
 __device__ __forceinline__ void store_half_row(__half* dst, const float* v) {
-  if constexpr (EPL == 8) {
-    uint32_t w[4];
+  uint32_t w[EPL / 2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h2 = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int i = 0; i < EPL / 2; ++i) {
+    __half2 h2 = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  if constexpr (EPL % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < EPL / 8; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   } else if constexpr (EPL == 4) {
-    __half2 a = __floats2half2_rn(v[0], v[1]);
-    __half2 b = __floats2half2_rn(v[2], v[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst) = u;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
   } else {
-    __half2 a = __floats2half2_rn(v[0], v[1]);
-    *reinterpret_cast<__half2*>(dst) = a;
+    *reinterpret_cast<uint32_t*>(dst) = w[0];
   }
 }
 
@@ -187,18 +190,25 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
   return ctx;
 }
 
+#ifndef PK_DECODE_FP8_RL
+#define PK_DECODE_FP8_RL 8
+#endif
+
 template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
 struct PartitionCfg {
-  // Lanes covering one token's D dims: 32 for fp16, 16 for e4m3 (two tokens
-  // per warp instruction, halving the shuffles per byte of the slimmer rows).
-  static constexpr int RL = FP8 ? 16 : 32;
-  static constexpr int NT = 32 / RL;                  // tokens per warp instruction
-  static constexpr int EPL = D / RL;                  // dims per lane
   // Tokens per pipeline stage: 16 fp16 rows (4 KB per head at D = 128), or 32
   // e4m3 rows at block size >= 16 -- the same bytes per stage, and every lane
   // then holds a distinct token's score, so the per-stage reductions cost half
   // as much per token.  A TMA box never spans blocks: TBX tokens, BPS per stage.
   static constexpr int TB = FP8 ? (BS >= 16 ? 32 : BS) : (BS < 16 ? BS : 16);
+  // Lanes covering one token's D dims: 32 for fp16; 8 for e4m3 (four tokens
+  // per warp instruction, 16 codes per lane: one 16-byte shared-memory read per
+  // token and lane, eight lanes per 128-byte row, so no bank conflicts; three
+  // butterfly rounds per stage instead of four at 16 lanes), at least 32 / TB so
+  // that a stage still fills one warp instruction.
+  static constexpr int RL = !FP8 ? 32 : (PK_DECODE_FP8_RL * TB >= 32 ? PK_DECODE_FP8_RL : 32 / TB);
+  static constexpr int NT = 32 / RL;                  // tokens per warp instruction
+  static constexpr int EPL = D / RL;                  // dims per lane
   static constexpr int TBX = TB < BS ? TB : BS;       // tokens per TMA box
   static constexpr int BPS = TB / TBX;                // boxes per tensor per stage
   static constexpr int SUB = BS / TBX;                // boxes per physical block
@@ -325,15 +335,14 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   // Query slice of this lane (and, for e4m3 pools, its fp16 pairs), read once
   // the first stages are in flight so that its latency overlaps the K/V copies.
-  float qf[EPL];
-  uint32_t qh[EPL / 2];
-  {
+  float qf[FP8 ? 1 : EPL];
+  uint32_t qh[FP8 ? EPL / 2 : 1];
+  if constexpr (FP8) {
+    load_words<EPL / 2>(qh, a.q + row_bh * D + dl);
+  } else {
     LaneVec<EPL> qv;
     qv.load(a.q + row_bh * D + dl);
     qv.to_float(qf);
-#pragma unroll
-    for (int e = 0; e < EPL / 2; ++e)
-      qh[e] = reinterpret_cast<const uint32_t*>(a.q + row_bh * D + dl)[e];
   }
 
   float m = -INFINITY, l = 0.f;
@@ -359,9 +368,9 @@ __global__ void __launch_bounds__(WARPS * 32)
 
     // Appending: the new token (position ctx-1) is scored from k_new/v_new,
     // copied over the stage row TMA brought in, and stored to its cache slot.
-    if (!FP8 && a.k_new != nullptr) {
+    if constexpr (!FP8) {
       const int t_new = ctx - 1 - (tok0 + i * TB);
-      if (t_new >= 0 && t_new < TB) {
+      if (a.k_new != nullptr && t_new >= 0 && t_new < TB) {
         const int pb = __shfl_sync(kFull, phys, i / SUB);
         const size_t src = row_bh * D + lane * EPL;
         LaneVec<EPL> kn, vn;
@@ -417,16 +426,12 @@ __global__ void __launch_bounds__(WARPS * 32)
     float dot = part_dot[0];
     if constexpr (FP8) dot *= kscl[Cfg::scale_index(my_tok)];  // per-(token, head) scale
     float sc = (my_tok < valid) ? dot * a.scale_log2 : -INFINITY;
-    float mb = sc;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
-    const float m_new = fmaxf(m, mb);
+    const float m_new = fmaxf(m, warp_max(sc));
     const float alpha = fast_exp2(m - m_new);
     const float pr = (my_tok < valid) ? fast_exp2(sc - m_new) : 0.f;
-    float psum = pr;
-#pragma unroll
-    for (int off = LPT; off <= 16; off <<= 1) psum += __shfl_xor_sync(kFull, psum, off);
-    l = l * alpha + psum;
+    // Each lane keeps the sum of its own tokens' weights (alpha is uniform
+    // over the warp); the lanes are summed once, after the last stage.
+    l = l * alpha + pr;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
     // e4m3 pools: the weight p * v_scale goes to fp16 (relative error 2^-11)
@@ -478,10 +483,14 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= 1.f / 256.f;  // exact
   }
-  if constexpr (RL < 32) {  // the two halves accumulated different tokens
+  // Lanes whose tokens differ: their weight sums, and (e4m3: several tokens
+  // per instruction) their o rows for the same dims.
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], 16);
-  }
+  for (int off = LPT; off <= 16; off <<= 1) l += __shfl_xor_sync(kFull, l, off);
+#pragma unroll
+  for (int off = RL; off < 32; off <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], off);
   const int n_parts = (ctx + a.part_tokens - 1) / a.part_tokens;
   if (n_parts == 1) {
     const float inv = 1.f / l;
@@ -493,11 +502,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     const size_t row = row_bh * a.num_parts + part;
     float* dst = a.ws_o + row * D + dl;
     if (lane < RL) {
-      if constexpr (EPL == 8) {
-        *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
-      } else if constexpr (EPL == 4) {
-        *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+      if constexpr (EPL % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < EPL / 4; ++i)
+          reinterpret_cast<float4*>(dst)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
       } else {
         *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
       }
