@@ -23,8 +23,11 @@
  * --------------------------------
  *  - fp16 data (pa_half) is IEEE binary16, passed as raw 16-bit patterns.
  *  - Every pointer argument except the host-side scalars is a DEVICE pointer
- *    of the current CUDA device, row-major and contiguous.  The caller owns
- *    all memory; the library allocates nothing and never synchronises.
+ *    of the current CUDA device, row-major and contiguous.  Where a call says
+ *    so, an argument may instead be the device address of mapped page-locked
+ *    host memory (pa_host_device_pointer): the kernel then reads or writes
+ *    it across the host link itself.  The caller owns all memory; the
+ *    library allocates nothing and never synchronises.
  *  - Every call is asynchronous on `stream` (0 = the legacy default stream).
  *  - Argument errors are reported synchronously, before anything is
  *    launched: PA_ERR_INVALID for a bad pointer, size or alignment,
@@ -77,6 +80,16 @@ int pa_last_cuda_error(void);
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int pa_version(void);
 
+/* Device address of page-locked host memory: memory from cudaHostAlloc /
+ * cudaMallocHost, or registered with cudaHostRegister, that is mapped into
+ * the current device's address space (always so with unified addressing).
+ * The device address lets a kernel load and store that memory directly,
+ * with no staging copy.  host_ptr may point anywhere inside the
+ * allocation.  Returns PA_ERR_INVALID, with *device_ptr set to NULL, when
+ * host_ptr is NULL or is not mapped page-locked memory; device_ptr must not
+ * be NULL.  Synchronous, launches nothing. */
+pa_status pa_host_device_pointer(const void *host_ptr, void **device_ptr);
+
 /* ---------------------------------------------------------------------------
  * Decode attention (one query token per sequence).
  *
@@ -100,7 +113,9 @@ int pa_version(void);
  * out          [B, H, D] fp16, written with round-to-nearest-even from an
  *              fp32 accumulation
  * D in {64, 128}; block_size in {4, 8, 16, 32}; q, k_cache, v_cache and out
- * 16-byte aligned.
+ * 16-byte aligned.  q, out, block_tables and context_lens may be mapped
+ * page-locked host memory (pa_host_device_pointer); the caches and the
+ * workspace are device memory.
  *
  * Long contexts are split into partitions of `partition_tokens` keys (a
  * multiple of block_size, at most 32 blocks; 0 picks one from B, H and
@@ -214,7 +229,9 @@ pa_status pa_shared_prefix_groups(const int32_t *block_tables,
  * pa_kv_cache_write + pa_decode.  Every other argument, the workspace and
  * the errors are as for pa_decode; a block id outside [0, num_blocks) for
  * the new token's block skips its store and sets PA_DEV_BAD_BLOCK_ID.
- * k_new and v_new must not alias the caches.
+ * k_new and v_new must not alias the caches; like q, out, block_tables
+ * and context_lens they may be mapped page-locked host memory (16-byte
+ * aligned).
  * ------------------------------------------------------------------------- */
 pa_status pa_decode_append(const pa_half *q, const pa_half *k_new,
                            const pa_half *v_new, pa_half *k_cache,

@@ -21,7 +21,7 @@ PA_DEV_TIMEOUT = 0x10
 
 # Every symbol include/pagedkv.h declares.
 EXPORTS = (
-    "pa_status_string", "pa_last_cuda_error", "pa_version",
+    "pa_status_string", "pa_last_cuda_error", "pa_version", "pa_host_device_pointer",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
     "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
     "pa_decode_static",
@@ -52,6 +52,8 @@ def _bind(lib):
     lib.pa_last_cuda_error.restype = _I
     lib.pa_version.argtypes = []
     lib.pa_version.restype = _I
+    lib.pa_host_device_pointer.argtypes = [_P, ctypes.POINTER(ctypes.c_void_p)]
+    lib.pa_host_device_pointer.restype = _I
     lib.pa_decode_partition_tokens.argtypes = [_I, _I, _I, _I]
     lib.pa_decode_partition_tokens.restype = _I
     lib.pa_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
@@ -136,6 +138,30 @@ def _need(t, dtype, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def host_device_pointer(t):
+    """Device address of a pinned CPU tensor's data (pa_host_device_pointer):
+    a kernel given it loads and stores the host memory directly."""
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("host_device_pointer takes a CPU tensor")
+    d = ctypes.c_void_p()
+    _check(lib().pa_host_device_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(d)),
+           "pa_host_device_pointer")
+    return d.value
+
+
+def _io(t, dtype, name, ndim):
+    """Pointer for a per-call input or output that the kernel may access in
+    place: a CUDA tensor, or a pinned CPU tensor (its mapped device address)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous() or t.dim() != ndim:
+            raise ValueError(f"{name} must be contiguous with {ndim} dims")
+        return ctypes.c_void_p(host_device_pointer(t))
+    _need(t, dtype, name, ndim)
+    return _ptr(t)
+
+
 def pa_decode_partition_tokens(B, H, block_size, max_context_len):
     return lib().pa_decode_partition_tokens(B, H, block_size, max_context_len)
 
@@ -150,31 +176,33 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_contex
     """Paged decode attention.  q [B,H,D] fp16; caches [NB,bs,H,D] fp16;
     block_tables [B,max_blocks] int32; context_lens [B] int32;
     ``max_context_len`` is a host-side upper bound on context_lens.
-    Returns ``out`` [B,H,D] fp16 (allocated when not given)."""
-    _need(q, torch.float16, "q", 3)
+    q, out, block_tables and context_lens may be pinned CPU tensors, read
+    and written by the kernels in place.  Returns ``out`` [B,H,D] fp16
+    (allocated on the device when not given)."""
+    qp = _io(q, torch.float16, "q", 3)
     _need(k_cache, torch.float16, "k_cache", 4)
     _need(v_cache, torch.float16, "v_cache", 4)
-    _need(block_tables, torch.int32, "block_tables", 2)
-    _need(context_lens, torch.int32, "context_lens", 1)
+    btp = _io(block_tables, torch.int32, "block_tables", 2)
+    clp = _io(context_lens, torch.int32, "context_lens", 1)
     B, H, D = q.shape
     NB, bs = k_cache.shape[0], k_cache.shape[1]
     if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
         raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
     if block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("block_tables/context_lens batch mismatch")
+    dev = k_cache.device
     if out is None:
-        out = torch.empty_like(q)
-    else:
-        _need(out, torch.float16, "out", 3)
+        out = torch.empty((B, H, D), dtype=torch.float16, device=dev)
+    op = _io(out, torch.float16, "out", 3)
     ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
                                         partition_tokens)
     if workspace is None and ws_bytes > 0:
-        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                         _ptr(context_lens), B, H, D, bs, NB, block_tables.shape[1],
-                         int(max_context_len), int(partition_tokens), float(scale), _ptr(out),
-                         _ptr(workspace), ws_len, _ptr(status), _stream(stream, q.device))
+    rc = lib().pa_decode(qp, _ptr(k_cache), _ptr(v_cache), btp, clp, B, H, D, bs, NB,
+                         block_tables.shape[1],
+                         int(max_context_len), int(partition_tokens), float(scale), op,
+                         _ptr(workspace), ws_len, _ptr(status), _stream(stream, dev))
     _check(rc, "pa_decode")
     return out
 
@@ -184,32 +212,36 @@ def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_le
                      stream=None):
     """Store each sequence's new token k_new/v_new [B,H,D] at position ctx-1
     of the paged cache and run decode attention including it (one launch).
-    Returns ``out`` [B,H,D] fp16."""
-    _need(q, torch.float16, "q", 3)
-    _need(k_new, torch.float16, "k_new", 3)
-    _need(v_new, torch.float16, "v_new", 3)
+    q, k_new, v_new, out, block_tables and context_lens may be pinned CPU
+    tensors, read and written by the kernels in place.  Returns ``out``
+    [B,H,D] fp16 (allocated on the device when not given)."""
+    qp = _io(q, torch.float16, "q", 3)
+    kp = _io(k_new, torch.float16, "k_new", 3)
+    vp = _io(v_new, torch.float16, "v_new", 3)
     _need(k_cache, torch.float16, "k_cache", 4)
     _need(v_cache, torch.float16, "v_cache", 4)
-    _need(block_tables, torch.int32, "block_tables", 2)
-    _need(context_lens, torch.int32, "context_lens", 1)
+    btp = _io(block_tables, torch.int32, "block_tables", 2)
+    clp = _io(context_lens, torch.int32, "context_lens", 1)
     B, H, D = q.shape
     NB, bs = k_cache.shape[0], k_cache.shape[1]
     if k_new.shape != q.shape or v_new.shape != q.shape:
         raise ValueError("k_new/v_new must be [B, H, D] like q")
     if tuple(k_cache.shape) != (NB, bs, H, D) or v_cache.shape != k_cache.shape:
         raise ValueError("k_cache/v_cache must be [num_blocks, block_size, H, D]")
+    dev = k_cache.device
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, H, D), dtype=torch.float16, device=dev)
+    op = _io(out, torch.float16, "out", 3)
     ws_bytes = pa_decode_workspace_size(B, H, D, bs, max(int(max_context_len), 1),
                                         partition_tokens)
     if workspace is None and ws_bytes > 0:
-        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
+        workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().pa_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                _ptr(block_tables), _ptr(context_lens), B, H, D, bs, NB,
+    rc = lib().pa_decode_append(qp, kp, vp, _ptr(k_cache), _ptr(v_cache), btp, clp,
+                                B, H, D, bs, NB,
                                 block_tables.shape[1], int(max_context_len),
-                                int(partition_tokens), float(scale), _ptr(out), _ptr(workspace),
-                                ws_len, _ptr(status), _stream(stream, q.device))
+                                int(partition_tokens), float(scale), op, _ptr(workspace),
+                                ws_len, _ptr(status), _stream(stream, dev))
     _check(rc, "pa_decode_append")
     return out
 

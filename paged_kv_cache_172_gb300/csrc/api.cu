@@ -122,6 +122,25 @@ int pa_last_cuda_error(void) { return g_last_cuda_error; }
 
 int pa_version(void) { return 100; }
 
+pa_status pa_host_device_pointer(const void* host_ptr, void** device_ptr) {
+  if (device_ptr == nullptr) return PA_ERR_INVALID;
+  *device_ptr = nullptr;
+  if (host_ptr == nullptr) return PA_ERR_INVALID;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, host_ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return PA_ERR_INVALID;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return PA_ERR_INVALID;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0) != cudaSuccess || !d) {
+    cudaGetLastError();
+    return PA_ERR_INVALID;
+  }
+  *device_ptr = d;
+  return PA_OK;
+}
+
 // ---------------------------------------------------------------------------
 // decode
 // ---------------------------------------------------------------------------

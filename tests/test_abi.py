@@ -121,3 +121,11 @@ def test_binding_rejects_cpu_tensors():
         pk.pa_decode(q, q.view(1, 1, 1, 64), q.view(1, 1, 1, 64),
                      torch.zeros(1, 1, dtype=torch.int32), torch.zeros(1, dtype=torch.int32),
                      0.1, max_context_len=1)
+
+
+def test_host_device_pointer_rejects_null_without_cuda(lib):
+    # NULL arguments are refused before any CUDA call
+    out = ctypes.c_void_p(0x1234)
+    assert lib.pa_host_device_pointer(NULL, ctypes.byref(out)) == pk.PA_ERR_INVALID
+    assert out.value is None
+    assert lib.pa_host_device_pointer(ctypes.c_void_p(0x1000), NULL) == pk.PA_ERR_INVALID
