@@ -33,7 +33,7 @@
 //    reads that slot.
 //  * A sequence that fits in one partition writes fp16 output directly;
 //    otherwise each partition writes (max, normaliser, unnormalised output)
-//    to the workspace and combine_kernel merges them by log-sum-exp.
+//    to the workspace and a combine kernel merges them by log-sum-exp.
 #include <math.h>
 
 #include <cuda_fp8.h>
@@ -516,13 +516,76 @@ __global__ void __launch_bounds__(WARPS * 32)
 
 // Log-sum-exp merge of the partitions of one (b, h):
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  out = sum_s 2^(m_s - M) o_s / L.
-// One CTA of W = blockDim.x / 32 warps per (b, h); warp w takes partitions
-// w, w + W, ...; lane l owns dims [l * D/32, (l+1) * D/32).  W grows with
-// the partition count so a 1M-token context (thousands of partitions) still
-// keeps many loads in flight; W == 1 for short contexts needs no CTA sync.
+// Up to kFastParts parts: combine_fast_kernel, one warp per (b, h).  More:
+// combine_kernel, one CTA of W = blockDim.x / 32 warps per (b, h); warp w
+// takes partitions w, w + W, ...; lane l owns dims [l * D/32, (l+1) * D/32).
+// W grows with the partition count so a 1M-token context (thousands of
+// partitions) still keeps many loads in flight.
 constexpr int kMaxCombineWarps = 16;
 constexpr int kFastParts = 16;  // combine: parts merged from registers by one warp
 
+constexpr int kCombineHeads = 4;  // fast combine: heads (one warp each) per CTA
+
+// At most kFastParts parts: one warp per (b, h), kCombineHeads heads per CTA
+// (one wave of CTAs even for a few thousand (b, h) pairs).  Every part's
+// (m, l) and output slice are loaded at once (slots past the sequence's
+// parts hold stale data and are masked), so the merge waits on one round
+// trip to L2 instead of two.
+template <int D>
+__global__ void __launch_bounds__(kCombineHeads * 32) combine_fast_kernel(const DecodeArgs a) {
+  constexpr int EPL = D / 32;
+  pdl_wait();  // partitions come from the partition kernel just before
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * kCombineHeads + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (h >= a.H) return;  // idle warp of a ragged head group (no CTA-wide sync)
+  const size_t row0 = ((size_t)b * a.H + h) * a.num_parts;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row0;
+  float2 mlv = make_float2(-INFINITY, 0.f);
+  if (lane < a.num_parts) mlv = ml[lane];
+  float ov[kFastParts][EPL];
+#pragma unroll
+  for (int s = 0; s < kFastParts; ++s) {
+    if (s < a.num_parts) {
+      const float* src = a.ws_o + (row0 + s) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(src);
+        ov[s][0] = t.x; ov[s][1] = t.y; ov[s][2] = t.z; ov[s][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(src);
+        ov[s][0] = t.x; ov[s][1] = t.y;
+      }
+    }
+  }
+  const int n = (checked_ctx(a, b, false) + a.part_tokens - 1) / a.part_tokens;
+  if (n <= 1) return;  // the partition kernel wrote the row itself
+  if (lane >= n) mlv = make_float2(-INFINITY, 0.f);
+  float mx = mlv.x;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+  const float wl = lane < n ? fast_exp2(mlv.x - mx) : 0.f;  // weight of part `lane`
+  float lsum = wl * mlv.y;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kFastParts; ++s) {
+    const float w = __shfl_sync(kFull, wl, s);
+    if (s < n) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, ov[s][e], acc[e]);
+    }
+  }
+  const float inv = 1.f / lsum;
+  float r[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = acc[e] * inv;
+  store_half_row<EPL>(a.out + ((size_t)b * a.H + h) * D + lane * EPL, r);
+}
+
+// More parts: one CTA of W = blockDim.x / 32 warps per (b, h).
 template <int D>
 __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
@@ -533,54 +596,6 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row0 = ((size_t)b * a.H + h) * a.num_parts;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row0;
-  if (W == 1 && a.num_parts <= kFastParts) {
-    // One warp, few parts: every part's (m, l) and output slice are loaded
-    // at once (slots past n hold stale data and are masked), so the merge
-    // waits on one round trip to L2 instead of two.
-    float2 mlv = make_float2(-INFINITY, 0.f);
-    if (lane < a.num_parts) mlv = ml[lane];
-    float ov[kFastParts][EPL];
-#pragma unroll
-    for (int s = 0; s < kFastParts; ++s) {
-      if (s < a.num_parts) {
-        const float* src = a.ws_o + (row0 + s) * D + lane * EPL;
-        if constexpr (EPL == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(src);
-          ov[s][0] = t.x; ov[s][1] = t.y; ov[s][2] = t.z; ov[s][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(src);
-          ov[s][0] = t.x; ov[s][1] = t.y;
-        }
-      }
-    }
-    const int n = (checked_ctx(a, b, false) + a.part_tokens - 1) / a.part_tokens;
-    if (n <= 1) return;  // the partition kernel wrote the row itself
-    if (lane >= n) mlv = make_float2(-INFINITY, 0.f);
-    float mx = mlv.x;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    const float wl = lane < n ? fast_exp2(mlv.x - mx) : 0.f;  // weight of part `lane`
-    float lsum = wl * mlv.y;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-    float acc[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-#pragma unroll
-    for (int s = 0; s < kFastParts; ++s) {
-      const float w = __shfl_sync(kFull, wl, s);
-      if (s < n) {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, ov[s][e], acc[e]);
-      }
-    }
-    const float inv = 1.f / lsum;
-    float r[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) r[e] = acc[e] * inv;
-    store_half_row<EPL>(a.out + ((size_t)b * a.H + h) * D + lane * EPL, r);
-    return;
-  }
   const int ctx = checked_ctx(a, b, false);
   const int n = (ctx + a.part_tokens - 1) / a.part_tokens;
   if (n <= 1) return;
@@ -725,7 +740,10 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
     e = launch_pdl(kern, grid, dim3(T::WARPS * 32), kSmem, stream, maps, a);
   }
   if (e != cudaSuccess) return e;
-  if (a.num_parts > 1) {
+  if (a.num_parts > 1 && a.num_parts <= kFastParts) {
+    e = launch_pdl(combine_fast_kernel<D>, dim3(a.B, (a.H + kCombineHeads - 1) / kCombineHeads),
+                   dim3(32 * kCombineHeads), 0, stream, a);
+  } else if (a.num_parts > 1) {
     int w = a.num_parts / 8;
     w = w < 1 ? 1 : (w > kMaxCombineWarps ? kMaxCombineWarps : w);
     e = launch_pdl(combine_kernel<D>, dim3(a.B, a.H), dim3(32 * w), 0, stream, a);
