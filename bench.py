@@ -43,10 +43,11 @@ L2_FLUSH_BYTES = 512 << 20
 # partition kernel (the dominant kernel) from an ncu capture of this bench's
 # 38-sequence batch, keyed by the hash of the decode source it was taken on;
 # null once the source changes.
-# (The second key: the same partition kernel, the file changed only in the
-# combine kernel.)
+# (Later keys: the same partition kernel; the file changed elsewhere -- the
+# combine kernel, the box-size rule shared with the maps.)
 DECODE_TRAFFIC = {"9567fb4ba38dcdb0": 853235456 + 5994752,
-                  "ca9f4bc9ad9c7b93": 853235456 + 5994752}
+                  "ca9f4bc9ad9c7b93": 853235456 + 5994752,
+                  "c9210cf186a5438a": 853235456 + 5994752}
 # The same for one launch of the chunked-prefill kernel (8 x 512 queries on
 # 3,584 cached tokens, block size 16), keyed by the hash of the prefill source.
 PREFILL_TRAFFIC = {("167764288f8a5ffe", 16): 713364224 + 46671872}

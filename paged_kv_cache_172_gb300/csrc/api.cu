@@ -249,9 +249,7 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   const long long rows = (long long)num_blocks * block_size;
   pk::DecodeMaps maps;
   memset(&maps, 0, sizeof(maps));
-  // tokens per TMA box of the decode stages: 16 fp16 rows; a whole block of
-  // e4m3 rows (a stage then spans 32 tokens)
-  const int box_tokens = fp8 != nullptr ? block_size : (block_size < 16 ? block_size : 16);
+  const int box_tokens = pk::decode_box_tokens(fp8 != nullptr, block_size);
   cudaError_t e;
   if (fp8 == nullptr) {
     e = pk::make_pool_map(&maps.k, k_cache, rows, H, D, 1, box_tokens);

@@ -193,6 +193,18 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
 #ifndef PK_DECODE_FP8_RL
 #define PK_DECODE_FP8_RL 8
 #endif
+#ifndef PK_DECODE_FP8_TB
+#define PK_DECODE_FP8_TB 32  // e4m3 tokens per stage at block size >= 16
+#endif
+
+// Tokens per TMA box of a stage (the maps' box): 16 fp16 rows; e4m3 rows up
+// to the stage size (the whole block at the default 32-token stages); below
+// block size 16, one block.
+constexpr int box_tokens_for(bool fp8, int bs) {
+  return (fp8 ? (bs >= 16 ? PK_DECODE_FP8_TB : bs) : (bs < 16 ? bs : 16)) < bs
+             ? (fp8 ? (bs >= 16 ? PK_DECODE_FP8_TB : bs) : (bs < 16 ? bs : 16))
+             : bs;
+}
 
 template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
 struct PartitionCfg {
@@ -200,7 +212,7 @@ struct PartitionCfg {
   // e4m3 rows at block size >= 16 -- the same bytes per stage, and every lane
   // then holds a distinct token's score, so the per-stage reductions cost half
   // as much per token.  A TMA box never spans blocks: TBX tokens, BPS per stage.
-  static constexpr int TB = FP8 ? (BS >= 16 ? 32 : BS) : (BS < 16 ? BS : 16);
+  static constexpr int TB = FP8 ? (BS >= 16 ? PK_DECODE_FP8_TB : BS) : (BS < 16 ? BS : 16);
   // Lanes covering one token's D dims: 32 for fp16; 8 for e4m3 (four tokens
   // per warp instruction, 16 codes per lane: one 16-byte shared-memory read per
   // token and lane, eight lanes per 128-byte row, so no bank conflicts; three
@@ -210,6 +222,7 @@ struct PartitionCfg {
   static constexpr int NT = 32 / RL;                  // tokens per warp instruction
   static constexpr int EPL = D / RL;                  // dims per lane
   static constexpr int TBX = TB < BS ? TB : BS;       // tokens per TMA box
+  static_assert(TBX == box_tokens_for(FP8, BS), "the maps' box is one stage box");
   static constexpr int BPS = TB / TBX;                // boxes per tensor per stage
   static constexpr int SUB = BS / TBX;                // boxes per physical block
   static constexpr int ELEM = FP8 ? 1 : 2;            // bytes per stored K/V element
@@ -757,6 +770,8 @@ bool prefix_supported(int D, int block_size, int max_group_size) {
   return (D == 64 || D == 128) && (block_size == 16 || block_size == 32) &&
          max_group_size >= 1 && max_group_size <= pfx::kMaxMembers;
 }
+
+int decode_box_tokens(bool fp8, int block_size) { return box_tokens_for(fp8, block_size); }
 
 bool decode_supported(int D, int block_size) {
   return (D == 64 || D == 128) &&

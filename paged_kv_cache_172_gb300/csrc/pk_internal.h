@@ -74,6 +74,9 @@ cudaError_t make_map_5d(CUtensorMap* map, const void* base, const unsigned long 
 // prefix partitions (multi-query, from maps.ksw / maps.vsw).
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream);
 bool decode_supported(int D, int block_size);
+// Tokens per TMA box of the decode partition kernel's stages (the box of the
+// K/V and scale maps must match it).
+int decode_box_tokens(bool fp8, int block_size);
 bool prefix_supported(int D, int block_size, int max_group_size);
 
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,
