@@ -132,8 +132,8 @@ class TinySchedule:
     """Inputs of the tiny replay.  Tables are NOT precomputed: the replay
     runs an allocator over ``free_order``.  ``k_tok[b]``/``v_tok[b]`` hold
     the K/V of every position of sequence b ([final_len, H, D]);
-    ``queries[r]`` is the [B, H, D] query batch attended after round r
-    (round 0 = right after prefill)."""
+    ``queries[r]`` is the [B, H, D] query batch attended after decode step r
+    (step 0 = right after prefill)."""
     B: int
     H: int
     D: int
@@ -158,8 +158,8 @@ def tiny_schedule(seed: int = 0, device="cpu") -> TinySchedule:
     final = [p + d for p, d in zip(prompt_lens, decode_steps)]
     k_tok = [randn16((n, H, D), g, device) for n in final]
     v_tok = [randn16((n, H, D), g, device) for n in final]
-    rounds = max(decode_steps)
-    queries = [randn16((B, H, D), g, device) for _ in range(rounds + 1)]
+    steps = max(decode_steps)
+    queries = [randn16((B, H, D), g, device) for _ in range(steps + 1)]
     return TinySchedule(B, H, D, bs, NB, free_order, prompt_lens, decode_steps,
                         k_tok, v_tok, queries, 1.0 / math.sqrt(D))
 
