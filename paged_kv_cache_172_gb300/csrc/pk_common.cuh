@@ -111,6 +111,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier `id` over `nthreads` threads that also ANDs a predicate: every
+// participant gets true only if all of them passed true.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // 5-D tiled TMA load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* map, int c0,
                                             int c1, int c2, int c3, int c4, uint64_t* bar) {

@@ -531,6 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&p_full[x]);
     }
     if (ok && ntile > 0) ok = __all_sync(kFull, mbar_wait(&pv_done[x], (ntile - 1) & 1));
+    // One decision for the whole tile (a wait that gave up in one warp only
+    // must not leave the others at the epilogue's barrier).
+    ok = named_bar_and(1 + x, 128, ok);
     if (ok && part >= 0) {
       // Part of a split unit: the unnormalised row (o, m, l) for the combine;
       // a Q tile with no key tile in this part leaves an empty partial.
