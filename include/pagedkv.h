@@ -290,14 +290,17 @@ pa_status pa_decode_fp8(const pa_half *q, const uint8_t *k_cache8,
  * in a fixed device array inside the library (PA_DECODE_STATIC_SCRATCH_BYTES,
  * held on every GPU that loads the library until the process exits).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
- *  - A plan needing more scratch than the array holds, i.e.
+ *  - Arguments are checked as pa_decode checks them, with the same codes;
+ *    then a plan needing more scratch than the array holds, i.e.
  *    pa_decode_workspace_size(...) > PA_DECODE_STATIC_SCRATCH_BYTES, is
  *    refused with PA_ERR_WORKSPACE before anything is launched; a smaller
  *    partition count (larger partition_tokens) or batch fits.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make
  *    that first call before any stream capture.  A failed look-up returns
- *    PA_ERR_CUDA.
+ *    PA_ERR_CUDA.  The cached address belongs to the device's current
+ *    context: after cudaDeviceReset on a device, do not call this entry
+ *    point on that device again in the same process.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero.  Calls whose kernels overlap on
  *    the GPU (different streams without ordering) race on it: serialise them.

@@ -49,9 +49,10 @@ def _compile(src, extra, obj_dir):
     return obj, r.stderr if "warning" in r.stderr.lower() else None
 
 
-def build(verbose: bool = False, extra_flags=(), out=None) -> str:
+def build(verbose: bool = False, extra_flags=(), out=None, sources=None) -> str:
     """Compile and link.  ``extra_flags`` (e.g. -D tuning macros) build a
-    variant with its own object directory; ``out`` names its library path."""
+    variant with its own object directory; ``out`` names its library path;
+    ``sources`` (file names in csrc/) limits a variant to those files."""
     extra_flags = tuple(extra_flags)
     lib = out or LIB
     obj_dir = OBJ_DIR
@@ -59,7 +60,10 @@ def build(verbose: bool = False, extra_flags=(), out=None) -> str:
         tag = hashlib.sha256(" ".join(extra_flags).encode()).hexdigest()[:10]
         obj_dir = os.path.join(OBJ_DIR, "variant_" + tag)
     os.makedirs(obj_dir, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    if sources is None:
+        srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    else:
+        srcs = [os.path.join(CSRC, s) for s in sources]
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         results = list(ex.map(lambda s: _compile(s, list(extra_flags), obj_dir), srcs))
     errors = [msg for _, msg in results if msg and "error" in msg.lower()]

@@ -53,6 +53,23 @@ namespace pk {
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
+int sm_count() {
+  static std::atomic<int> cached[64];  // per device; 0 = not queried yet
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const bool slot = dev >= 0 && dev < 64;
+  if (slot && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 cudaError_t make_pool_map(CUtensorMap* map, const void* base, long long rows, int H, int D,
                           int box_heads, int box_tokens) {
   auto fn = encode_fn();

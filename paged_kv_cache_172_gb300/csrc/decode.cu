@@ -731,25 +731,17 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
   bool grouped = false;
   if constexpr (!FP8 && BS % 16 == 0) grouped = a.seq_group != nullptr;
   if (!grouped) {
-    auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
-    static bool attr_done = false;  // per process: the attribute belongs to the function
-    if (!attr_done) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-      attr_done = true;
-    }
+    constexpr auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
+    e = ensure_dynamic_smem<kern>(Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
   } else if constexpr (!FP8 && BS % 16 == 0) {
     // The grouped grid also runs the shared-prefix partitions.
     constexpr int kPfxSmem = pfx::PrefixCfg<D, T::WARPS>::SMEM;
     constexpr int kSmem = Cfg::SMEM_BYTES > kPfxSmem ? Cfg::SMEM_BYTES : kPfxSmem;
-    auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8, true>;
-    static bool attr_done = false;
-    if (!attr_done) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      attr_done = true;
-    }
+    constexpr auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8, true>;
+    e = ensure_dynamic_smem<kern>(kSmem);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(kern, grid, dim3(T::WARPS * 32), kSmem, stream, maps, a);
   }
   if (e != cudaSuccess) return e;

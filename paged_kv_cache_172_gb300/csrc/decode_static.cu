@@ -57,12 +57,19 @@ extern "C" pa_status pa_decode_static(const pa_half* q, const pa_half* k_cache,
                                       int block_size, int num_blocks, int max_blocks_per_seq,
                                       int max_context_len, int partition_tokens, float scale,
                                       pa_half* out, int32_t* status, pa_stream_t stream) {
-  // Size check first: a plan that needs more scratch than the fixed array
-  // holds is refused before anything touches the device.
   const size_t need = pa_decode_workspace_size(B, H, D, block_size,
                                                max_context_len > 0 ? max_context_len : 1,
                                                partition_tokens);
-  if (need > PA_DECODE_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+  if (need > PA_DECODE_STATIC_SCRATCH_BYTES) {
+    // The plan does not fit the array.  pa_decode without a workspace checks
+    // every argument first (an unsupported head_dim or block size, a bad
+    // partition size, a null pointer ...) and returns that code; for a call
+    // whose arguments are all valid it returns PA_ERR_WORKSPACE.  Either way
+    // it returns before any launch.
+    return pa_decode(q, k_cache, v_cache, block_tables, context_lens, B, H, D, block_size,
+                     num_blocks, max_blocks_per_seq, max_context_len, partition_tokens, scale,
+                     out, nullptr, 0, status, stream);
+  }
   void* ws = nullptr;
   if (need > 0) {
     cudaError_t e = cudaSuccess;

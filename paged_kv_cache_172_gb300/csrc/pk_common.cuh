@@ -13,8 +13,13 @@ namespace pk {
 
 // A bounded wait gives up after this many SM clock cycles (about 1 s at
 // 2 GHz): far above any legitimate TMA latency, short enough that a lost
-// transaction returns control to the host instead of hanging the GPU.
-constexpr long long kWaitLimitCycles = 2000000000LL;
+// transaction returns control to the host instead of hanging the GPU.  A
+// build may set a shorter limit (PK_WAIT_LIMIT_CYCLES) for the test hook that
+// makes a wait run out on purpose.
+#ifndef PK_WAIT_LIMIT_CYCLES
+#define PK_WAIT_LIMIT_CYCLES 2000000000LL
+#endif
+constexpr long long kWaitLimitCycles = PK_WAIT_LIMIT_CYCLES;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

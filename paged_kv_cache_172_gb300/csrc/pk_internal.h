@@ -8,9 +8,32 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pagedkv.h"
 
 namespace pk {
+
+// Sets Kern's dynamic shared-memory limit on the current device the first
+// time it is launched there.  The attribute belongs to the function as loaded
+// on one device, so it is tracked per device; two threads that race on a
+// device's first launch may both set it, which is harmless.
+template <auto Kern>
+cudaError_t ensure_dynamic_smem(int bytes) {
+  static std::atomic<unsigned long long> done{0};  // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// Multiprocessor count of the current device (cached per device; 0 when the
+// query fails).
+int sm_count();
 
 // Makes `e` the value pa_last_cuda_error() reports on this thread.
 void record_cuda_error(cudaError_t e);

@@ -675,17 +675,6 @@ __global__ void __launch_bounds__(256)
   *reinterpret_cast<uint2*>(a.out + (((size_t)b * a.H + h) * a.Lq + qi) * kD + lane * 4) = u;
 }
 
-int sm_count() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      cached = n;
-  }
-  return cached;
-}
-
 #ifndef PK_PREFILL_MAX_SPLIT
 #define PK_PREFILL_MAX_SPLIT 4  // key ranges per split unit at most (swept: 2..8)
 #endif
@@ -753,13 +742,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
     e = make_map_5d(&vmap, v_cache, dims, strides, box, true);
     if (e != cudaSuccess) return e;
   }
-  auto kern = prefill_kernel<BS>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  constexpr auto kern = prefill_kernel<BS>;
+  e = ensure_dynamic_smem<kern>(kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.full_units + (plan.units - plan.full_units) * plan.split);
   cfg.blockDim = dim3(kThreads);

@@ -75,6 +75,30 @@ def test_decode_validation(lib):
     assert decode_rc(lib, pt=16, ws=0x1000, wsb=16) == pk.PA_ERR_WORKSPACE
 
 
+def static_rc(lib, **kw):
+    a = dict(q=0x1000, k=0x1000, v=0x1000, bt=0x1000, cl=0x1000, B=64, H=40, D=128, bs=16,
+             nb=8, maxb=128, maxctx=2048, pt=32, scale=0.1, out=0x1000, status=NULL)
+    a.update(kw)
+    return lib.pa_decode_static(a["q"], a["k"], a["v"], a["bt"], a["cl"], a["B"], a["H"],
+                                a["D"], a["bs"], a["nb"], a["maxb"], a["maxctx"], a["pt"],
+                                a["scale"], a["out"], a["status"], NULL)
+
+
+def test_decode_static_validation_matches_decode(lib):
+    # 64 x 40 x 64 partitions: far more scratch than the fixed array holds.
+    assert pk.pa_decode_workspace_size(64, 40, 128, 16, 2048, 32) > \
+        pk._lib.PA_DECODE_STATIC_SCRATCH_BYTES
+    assert static_rc(lib) == pk.PA_ERR_WORKSPACE
+    # An argument error gets pa_decode's code even when the plan is oversized.
+    assert static_rc(lib, D=256) == pk.PA_ERR_UNSUPPORTED
+    assert static_rc(lib, bs=12, pt=36) == pk.PA_ERR_UNSUPPORTED
+    assert static_rc(lib, pt=24) == pk.PA_ERR_INVALID  # not a block multiple
+    assert static_rc(lib, q=NULL) == pk.PA_ERR_INVALID
+    assert static_rc(lib, maxctx=4096) == pk.PA_ERR_INVALID  # beyond table capacity
+    assert static_rc(lib, scale=float("inf")) == pk.PA_ERR_INVALID
+    assert static_rc(lib, B=0) == pk.PA_OK
+
+
 def test_workspace_plan(lib):
     # 4 partitions of 16 tokens for max context 64, per (b, h): D + 2 floats
     assert pk.pa_decode_workspace_size(2, 4, 128, 16, 64, 16) == 2 * 4 * 4 * 130 * 4

@@ -71,6 +71,29 @@ def test_static_scratch_matches_workspace_path_twice():
         assert torch.all(out[5] == 0)  # empty sequence
 
 
+def test_static_single_partition_and_empty_batch():
+    # One partition (partition_tokens >= max_context_len): no scratch is
+    # needed and the array is not touched; then a batch whose contexts are
+    # all 0 (max_context_len 0 is planned as 1).  Both against pa_decode.
+    for ctx, max_ctx, pt in (([300, 1, 512, 77], 512, 512), ([0, 0, 0], 0, 0)):
+        batch = workloads.random_decode(len(ctx), 4, 128, 16, ctx, seed=41, device=DEV,
+                                        extra_blocks=2)
+        g = {k: getattr(batch, k) for k in ("q", "k_cache", "v_cache", "block_tables",
+                                            "context_lens")}
+        assert pk.pa_decode_workspace_size(len(ctx), 4, 128, 16, max(max_ctx, 1), pt) == 0
+        ref = pk.pa_decode(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                           g["context_lens"], batch.scale, max_ctx, partition_tokens=pt)
+        out = torch.full_like(g["q"], float("nan"))
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        rc = call_static(g, batch, max_ctx, pt, out, status)
+        assert rc == pk.PA_OK, pk.status_string(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out, ref)  # same kernel, same plan: identical bits
+        if max_ctx == 0:
+            assert torch.all(out == 0)
+
+
 def test_static_scratch_rejects_oversized_plan():
     # 64 sequences x 40 heads x 64 partitions of 32 tokens x (128 + 2) floats
     # is 85 MB of scratch, more than the fixed array holds: refused before launch.
