@@ -50,7 +50,6 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
-CLOCK_WINDOW_S = 0.5  # back-to-back steps sampled for the clock record
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of a workload's
 # dominant kernel, from one ncu capture (profiles/), keyed by the workload, the
@@ -464,7 +463,7 @@ def run_gpu(args, rank, world, local_rank, sampler):
     total_ms = sum(step_ms)
     # the clock window: the same step back to back (sampled, not the headline)
     _, _, cwin, sustained = timed_steps([("step", step)], stream, flush, 1, 1,
-                                        sustain_s=CLOCK_WINDOW_S)
+                                        sustain_s=args.clock_window_s)
     windows += cwin[1:]
 
     # -- the same step as two launches (cache write, then decode), for reference
@@ -811,7 +810,7 @@ def measure_workload(name, args, dev, sampler, peaks, cpu_budget_s):
     spec = SPECS[name](pk, workloads, dev, args, status, stream)
     torch.cuda.synchronize(dev)
     phase_ms, step_ms, windows, sustained = timed_steps(
-        spec["phases"], stream, flush, args.steps, args.warmup, sustain_s=CLOCK_WINDOW_S)
+        spec["phases"], stream, flush, args.steps, args.warmup, sustain_s=args.clock_window_s)
     alt_ms = {}
     for nm, fn in spec["alt"].items():  # alternatives timed beside the step, same flushing
         pm, _, w, _ = timed_steps([(nm, fn)], stream, flush, args.steps, args.warmup)
@@ -963,6 +962,9 @@ def main():
                     help="omit the other workloads from the default line")
     ap.add_argument("--block-size", type=int, default=16,
                     help="physical block size of the synthetic pools (16 or 32)")
+    ap.add_argument("--clock-window-s", type=float, default=0.5,
+                    help="seconds of back-to-back steps after each timed region, sampled for "
+                         "the clock record (0: none)")
     ap.add_argument("--context-len", type=int, default=1 << 20,
                     help="tokens of the long-context sequence (a smaller one for captures)")
     ap.add_argument("--workload", default="llama13b_decode",
