@@ -22,6 +22,8 @@ the tables alone took 6-8 us and staging everything ~20 us.  With
 beats five small ones), the kernel on the device copies, one device->host
 copy of the output.
 """
+import ctypes
+
 import torch
 
 from . import _lib
@@ -65,6 +67,7 @@ class DecodeSession:
                                            self.partition_tokens)
         self.workspace = torch.empty(max(ws // 4, 1) + 4, dtype=torch.float32, device=dev)
         self._h_stage = None
+        self._call_args = None  # pa_decode_append's arguments up to the workspace size
 
     def _views(self, buf):
         out = {}
@@ -82,7 +85,31 @@ class DecodeSession:
         self._h_stage = torch.empty(self._stage_bytes, dtype=torch.uint8, pin_memory=True)
         host = self._views(self._h_stage)
         host["out"] = torch.empty(self.out.shape, dtype=torch.float16, pin_memory=True)
+        self._call_args = self._marshal(host)
         return host
+
+    def _marshal(self, host):
+        """pa_decode_append's arguments (all but status and stream), built once:
+        the buffers never move, so each step skips the per-call argument checks
+        and the device-address look-ups of the pinned host buffers."""
+        P = ctypes.c_void_p
+        if self.zero_copy:
+            base = _lib.host_device_pointer(self._h_stage)
+            src = {name: P(base + off) for (name, _, _), off in zip(self._fields, self._offsets)}
+            out = P(_lib.host_device_pointer(host["out"]))
+        else:
+            src = {"q": P(self.q.data_ptr()), "k_new": P(self.k_new.data_ptr()),
+                   "v_new": P(self.v_new.data_ptr()),
+                   "context_lens": P(self.context_lens.data_ptr()),
+                   "block_tables": P(self.block_tables.data_ptr())}
+            out = P(self.out.data_ptr())
+        NB = self.k_cache.shape[0]
+        return (src["q"], src["k_new"], src["v_new"], P(self.k_cache.data_ptr()),
+                P(self.v_cache.data_ptr()), src["block_tables"], src["context_lens"],
+                self.B, self.H, self.D, self.bs, NB, self.block_tables.shape[1],
+                self.max_context_len, self.partition_tokens, ctypes.c_float(self.scale), out,
+                P(self.workspace.data_ptr()),
+                self.workspace.numel() * self.workspace.element_size())
 
     def h2d_bytes(self):
         """Bytes moved host -> device per step: the staged copy and, with
@@ -100,18 +127,16 @@ class DecodeSession:
         output lands in host['out'] when the stream reaches the end."""
         if self._h_stage is None or host["q"].data_ptr() != self._h_stage.data_ptr():
             raise ValueError("step_from_host takes the buffers returned by host_buffers()")
+        if stream is None:
+            stream = torch.cuda.current_stream(self.k_cache.device)
+        st = ctypes.c_void_p(None if status is None else status.data_ptr())
+        sp = ctypes.c_void_p(stream.cuda_stream)
         if self.zero_copy:
-            _lib.pa_decode_append(host["q"], host["k_new"], host["v_new"], self.k_cache,
-                                  self.v_cache, host["block_tables"], host["context_lens"],
-                                  self.scale, self.max_context_len, out=host["out"],
-                                  partition_tokens=self.partition_tokens,
-                                  workspace=self.workspace, status=status, stream=stream)
+            _lib._check(_lib.lib().pa_decode_append(*self._call_args, st, sp), "pa_decode_append")
             return host["out"]
-        self._d_stage.copy_(self._h_stage, non_blocking=True)
-        _lib.pa_decode_append(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
-                              self.block_tables, self.context_lens, self.scale,
-                              self.max_context_len, out=self.out,
-                              partition_tokens=self.partition_tokens, workspace=self.workspace,
-                              status=status, stream=stream)
-        host["out"].copy_(self.out, non_blocking=True)
+        with torch.cuda.stream(stream):
+            self._d_stage.copy_(self._h_stage, non_blocking=True)
+        _lib._check(_lib.lib().pa_decode_append(*self._call_args, st, sp), "pa_decode_append")
+        with torch.cuda.stream(stream):
+            host["out"].copy_(self.out, non_blocking=True)
         return host["out"]
