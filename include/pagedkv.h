@@ -329,10 +329,12 @@ pa_status pa_decode_static(const pa_half *q, const pa_half *k_cache,
  * q   [B, H, Lq, D] fp16 (the blog's [batch, heads, seq_len, head_dim])
  * out [B, H, Lq, D] fp16
  * context_lens[b] in [Lq, max_blocks_per_seq * block_size]; scale > 0.
- * D == 128 and block_size in {16, 32} run on the tcgen05 tensor-core kernel;
- * other supported (D, block_size) pairs return PA_ERR_UNSUPPORTED.  The pool
- * must hold fewer than 2^31 (slot, head) rows (num_blocks * block_size * H;
- * under 512 GiB per pool at D = 128), else PA_ERR_INVALID.
+ * D in {64, 128} and block_size in {4, 8, 16, 32}, all on the tcgen05
+ * tensor-core kernel (blocks of 8 or more tokens arrive by TMA; 4-token
+ * blocks are gathered with 16-byte copies, the slower path); any other
+ * (D, block_size) returns PA_ERR_UNSUPPORTED.  The pool must hold fewer
+ * than 2^31 (slot, head) rows (num_blocks * block_size * H; under 512 GiB
+ * per pool at D = 128), else PA_ERR_INVALID.
  *
  * workspace (device, 16-byte aligned, caller-owned, may be NULL): with at
  * least pa_prefill_workspace_size(B, H, Lq, D) bytes, the work units of the

@@ -441,8 +441,7 @@ pa_status pa_decode_append(const pa_half* q, const pa_half* k_new, const pa_half
 // chunked prefill
 // ---------------------------------------------------------------------------
 size_t pa_prefill_workspace_size(int B, int H, int Lq, int D) {
-  if (D != 128) return 0;
-  return pk::prefill_workspace_bytes(B, H, Lq);
+  return pk::prefill_workspace_bytes(B, H, Lq, D);
 }
 
 pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
@@ -462,7 +461,7 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
   // the prefill kernel addresses the pool by (slot, head) rows
   if ((long long)num_blocks * block_size * H >= (1LL << 31)) return PA_ERR_INVALID;
   if ((long long)Lq > (long long)max_blocks_per_seq * block_size) return PA_ERR_INVALID;
-  const size_t need = pk::prefill_workspace_bytes(B, H, Lq);
+  const size_t need = pk::prefill_workspace_bytes(B, H, Lq, D);
   if (workspace != nullptr && need > 0 && workspace_bytes < need) return PA_ERR_WORKSPACE;
   if (workspace != nullptr && !aligned16(workspace)) return PA_ERR_INVALID;
   pk::PrefillArgs a;

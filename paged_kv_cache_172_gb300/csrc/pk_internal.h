@@ -120,11 +120,13 @@ struct PrefillArgs {
   // Tail split (set by launch_prefill): CTAs [0, full_units) are whole units
   // (one per (sequence, head, 256-query pair), in that order, units gx * H * B);
   // each later unit's key tiles are split into `split` parts whose partials
-  // (kPrefillPartialStride floats per query row) go to ws and are merged by a
-  // combine kernel.
+  // (D + 4 floats per query row: o[D], m, l, pad) go to ws and are merged by
+  // a combine kernel.
   float* ws;
   size_t ws_floats;
   int gx, full_units, split;
+  const __half* k_cache;  // the pools (set by launch_prefill; read directly by
+  const __half* v_cache;  // the cp.async gather of blocks under 8 tokens)
   const int32_t* block_tables;
   const int32_t* context_lens;
   __half* out;
@@ -132,10 +134,9 @@ struct PrefillArgs {
   int B, H, Lq, D, block_size, num_blocks, max_blocks;
   float scale_log2;
 };
-constexpr int kPrefillPartialStride = 132;  // o[128], m, l, pad (16-byte aligned rows)
 bool prefill_supported(int D, int block_size);
 // Bytes of workspace the tail split needs on the current device (0: none).
-size_t prefill_workspace_bytes(int B, int H, int Lq);
+size_t prefill_workspace_bytes(int B, int H, int Lq, int D);
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                            cudaStream_t stream);
 

@@ -8,22 +8,27 @@
 // 0 .. n-Lq+i).
 //
 // One CTA = 256 queries (two 128-row tiles A and B) of one (sequence, head);
-// it walks the visible keys in tiles of 128 (8 blocks of 16 or 4 of 32):
+// it walks the visible keys in tiles of 128 (128 / block_size blocks):
 //   warps 0-3   softmax of tile A, one query row per thread (TMEM lane = row);
 //   warps 4-7   softmax of tile B;
-//   warp 8      TMA producer: Q (4 boxes of 128 rows x 64 dims, 128-byte
-//               swizzle), then per key tile one 5-D box per block (all its
-//               tokens, both 64-dim halves) for K and for V, gathered through
-//               the block table, into a 3-slot ring in first-use order K_0,
-//               K_1, V_0, K_2, V_1, ...;
+//   warp 8      producer: Q (boxes of 128 rows x 64 dims, 128-byte swizzle),
+//               then per key tile one 5-D TMA box per block (all its tokens,
+//               every 64-dim half) for K and for V, gathered through the
+//               block table, into a ring in first-use order K_0, K_1, V_0,
+//               K_2, V_1, ...  With 4-token blocks (half of an 8-row swizzle
+//               atom) the lanes gather the rows with 16-byte cp.async copies
+//               into the same layout instead;
 //   warp 9      S issuer (one thread) and tensor-memory owner;
 //   warp 10     P V issuer (one thread).
-// Tensor memory: S [0,128) shared by the two tiles, Q_A [128,192) and
-// Q_B [192,256) (fp16 pairs), O_A [256,384), O_B [384,512).  Q sits in tensor
-// memory (S = Q K^T takes its A operand from there) so that shared memory
-// holds a 5-slot K/V ring: with Q in shared memory only 3 slots fit and K/V
-// tiles landed late.  Q arrives by TMA in the P buffers, which are free until
-// the first P store; each softmax thread moves its row into tensor memory.
+// Head dims 128 and 64 are instantiations of the same kernel (D / 64 halves
+// of 64 dims; 128-byte swizzle rows of 64 fp16).
+// Tensor memory: S [0,128) shared by the two tiles, Q_A and Q_B from column
+// 128 (D/2 columns each, fp16 pairs), O_A and O_B from column 256 (D columns
+// each).  Q sits in tensor memory (S = Q K^T takes its A operand from there)
+// so that shared memory holds a deep K/V ring: with Q in shared memory only
+// 3 slots of 32 KB fit and K/V tiles landed late.  Q arrives by TMA in the P
+// buffers, which are free until the first P store; each softmax thread moves
+// its row into tensor memory.
 // Softmax of tile X, key tile j: wait for S_X(j), load the whole row into
 // registers and release S at once, so the tensor core computes the other
 // tile's S while this softmax still works on j.  Row max (keys past the row's position
@@ -40,15 +45,18 @@
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle; the
 // 16-byte chunk c of a 128-byte row r sits at chunk position c ^ (r mod 8)):
 //   Q (staged), P: K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B
-//                 apart, the two 64-element halves 16 KB apart;
-//   K_j, V_j    : key groups of 8 keys x 128 dims, 2 KB apart, each holding
-//                 the 1 KB atom of dims 0-63 then that of dims 64-127 (the
-//                 order one box of a block lands in).  K_j is read K-major
-//                 (8-key atoms 2 KB apart along N, halves 1 KB apart along
-//                 K), V_j MN-major (8-key atoms 2 KB apart along K, halves
-//                 1 KB apart along N).  Fewer, larger boxes: the TMA unit
-//                 spends a fixed ~50 cycles per box besides ~2 per 128-byte
-//                 row, which bounded the K/V stream at block size 16.
+//                 apart, 64-element halves 16 KB apart;
+//   K_j, V_j    : key groups of 8 keys x D dims (D * 16 bytes apart), each
+//                 holding the 1 KB atom of dims 0-63 then (D = 128) that of
+//                 dims 64-127 (the order one box of a block lands in).  K_j
+//                 is read K-major (8-key atoms one group apart along N, halves
+//                 1 KB apart along K), V_j MN-major (8-key atoms one group
+//                 apart along K, halves 1 KB apart along N).  Fewer, larger
+//                 boxes: the TMA unit spends a fixed ~50 cycles per box besides
+//                 ~2 per 128-byte row, which bounded the K/V stream at block
+//                 size 16.
+#include <string.h>
+
 #include "pk_common.cuh"
 #include "pk_internal.h"
 #include "pk_tcgen05.cuh"
@@ -60,11 +68,8 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTileM = 128;                  // queries per Q tile (two per CTA)
 constexpr int kTileN = 128;                  // keys per tile
-constexpr int kD = 128;                      // head dim
-constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16
-constexpr int kTileBytes = 2 * kSlabBytes;   // 128 rows x 128 fp16
-constexpr int kGroupBytes = 2048;            // K/V tiles: 8 keys x 128 dims
-constexpr int kStages = 5;                   // K/V ring, tiles in first-use order
+constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16 (a P or staged-Q half)
+constexpr int kPTileBytes = 2 * kSlabBytes;  // P: 128 queries x 128 keys fp16
 constexpr int kThreads = 352;                // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                  // S = Q K^T issuer, tensor-memory owner
@@ -72,25 +77,39 @@ constexpr int kWarpPv = 10;                  // O += P V issuer
 constexpr int kTblWindow = 256;              // block-table entries staged in smem
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColQ = 128;              // Q_A, then Q_B 64 columns later
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 128;              // Q_A, then Q_B D/2 columns later
+constexpr uint32_t kColO = 256;              // O_A, then O_B D columns later
+constexpr int kMaxStages = 8;
+constexpr int kNumBars = 1 + 2 * kMaxStages + 2 + 2 + 2 + 2 + 1 + 2;
 
-constexpr int kOffP = 0;                                // P_A, P_B (Q staged first)
-constexpr int kOffKV = kOffP + 2 * kTileBytes;
-constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2;
-constexpr int kOffTmemHolder = kOffBar + kNumBars * 8;
-constexpr int kOffIssued = kOffTmemHolder + 4;          // [2] S products issued per tile
-constexpr int kOffTbl = (kOffIssued + 8 + 15) / 16 * 16;
-constexpr int kSmemBytes = kOffTbl + kTblWindow * 4 + 1024;  // + alignment slack
+// Per head dim: the K/V tile (128 keys x D dims), its 8-key groups, and the
+// ring depth that fills the shared memory the two P tiles leave.
+template <int D>
+struct PfCfg {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int HALVES = D / 64;                 // 64-dim halves of a row
+  static constexpr int TILE_BYTES = kTileN * D * 2;     // one K or V tile (= one Q tile)
+  static constexpr int GROUP_BYTES = 8 * D * 2;         // 8 keys x D dims
+  static constexpr int STAGES = D == 128 ? 5 : 8;       // K/V ring slots
+  static_assert(STAGES <= kMaxStages, "barrier room");
+  static constexpr int OFF_P = 0;                       // P_A, P_B (Q staged first)
+  static constexpr int OFF_KV = OFF_P + 2 * kPTileBytes;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
+  static constexpr int OFF_TMEM_HOLDER = OFF_BAR + kNumBars * 8;
+  static constexpr int OFF_ISSUED = OFF_TMEM_HOLDER + 4;  // [2] S products issued per tile
+  static constexpr int OFF_TBL = (OFF_ISSUED + 8 + 15) / 16 * 16;
+  static constexpr int SMEM_BYTES = OFF_TBL + kTblWindow * 4 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static constexpr uint32_t IDESC_S = tc::idesc_f16_f32(kTileM, kTileN, false, false);
+  static constexpr uint32_t IDESC_O = tc::idesc_f16_f32(kTileM, D, false, true);
+  static constexpr uint32_t TILE_DESC = TILE_BYTES >> 4;  // one K/V tile, descriptor units
+  static constexpr int PARTIAL_STRIDE = D + 4;            // o[D], m, l, pad (16-byte rows)
+};
 
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr uint32_t kIdescS = tc::idesc_f16_f32(kTileM, kTileN, false, false);
-constexpr uint32_t kIdescO = tc::idesc_f16_f32(kTileM, kD, false, true);
-constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one tile, in descriptor address units
+constexpr uint32_t kPTileDesc = kPTileBytes >> 4;  // one P tile, descriptor units
 
 // Descriptor address offset of K step kk (16 elements = 32 B) of a K-major
-// Q or P tile: inside the 64-element half kk / 4.
+// P tile: inside the 64-element half kk / 4.
 __device__ __forceinline__ constexpr uint32_t kmajor_off(int kk) {
   return (uint32_t)((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
 }
@@ -99,8 +118,9 @@ __device__ __forceinline__ constexpr uint32_t kgroup_off(int kk) {
   return (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
 }
 // ... of an MN-major V tile: keys 16*kk .. 16*kk+15 are two key groups.
+template <int D>
 __device__ __forceinline__ constexpr uint32_t vmn_off(int kk) {
-  return (uint32_t)(kk * 2 * kGroupBytes) >> 4;
+  return (uint32_t)(kk * 2 * PfCfg<D>::GROUP_BYTES) >> 4;
 }
 
 // Wait until the S issuer has issued `n` S products of a tile (its counter
@@ -119,21 +139,41 @@ __device__ __forceinline__ bool wait_issued(volatile int* cnt, int n) {
 __device__ __forceinline__ int load_k(int t) { return t == 0 ? 0 : 2 * t - 1; }
 __device__ __forceinline__ int load_v(int t, int n_kv) { return t + 1 < n_kv ? 2 * t + 2 : 2 * t + 1; }
 
-template <int BS>
+// 16-byte asynchronous global -> shared copy (cached in L2 only), in the
+// thread's current cp.async group.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap,
                    const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
-  constexpr int BPT = kTileN / BS;  // blocks per key tile
+  using C = PfCfg<D>;
+  constexpr int BPT = kTileN / BS;    // blocks per key tile
+  constexpr bool kGatherCp = BS < 8;  // a block is less than one 8-row swizzle atom
+  constexpr int kStages = C::STAGES;
+  constexpr int kTileBytes = C::TILE_BYTES;
+  constexpr int kGroupBytes = C::GROUP_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
-  uint8_t* sQ = smem + kOffP;  // staging only
-  uint8_t* sP = smem + kOffP;
-  uint8_t* sKV = smem + kOffKV;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint8_t* sQ = smem + C::OFF_P;  // staging only
+  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sKV = smem + C::OFF_KV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
@@ -143,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + 2;         // [2]: O_X += P_X(j) V_j completed
   uint64_t* drain = pv_done + 2;
   uint64_t* q_ready = drain + 1;          // [2]: Q_X moved into tensor memory
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffTmemHolder);
-  int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + kOffTbl);
-  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_HOLDER);
+  int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + C::OFF_TBL);
+  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + C::OFF_ISSUED);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -160,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Partial rows of this part (query row r of the unit at ws_part + r * stride).
   float* ws_part = part < 0 ? nullptr
                             : a.ws + ((size_t)(unit - a.full_units) * a.split + part) *
-                                         (2 * kTileM) * kPrefillPartialStride;
+                                         (2 * kTileM) * C::PARTIAL_STRIDE;
 
   pdl_wait();  // inputs may come from the previous kernel on the stream
   const int n = a.context_lens[b];
@@ -170,13 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n < a.Lq || n > a.max_blocks * BS) {
     if (threadIdx.x == 0 && part <= 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
     if (part < 0) {
-      uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * kD);
-      for (int i = threadIdx.x; i < rows_all * (kD / 8); i += kThreads)
+      uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * D);
+      for (int i = threadIdx.x; i < rows_all * (D / 8); i += kThreads)
         o4[i] = make_uint4(0, 0, 0, 0);
     } else {  // an empty partial: the combine writes zero rows
       for (int r = threadIdx.x; r < 2 * kTileM; r += kThreads) {
-        ws_part[(size_t)r * kPrefillPartialStride + kD] = -INFINITY;
-        ws_part[(size_t)r * kPrefillPartialStride + kD + 1] = 0.f;
+        ws_part[(size_t)r * C::PARTIAL_STRIDE + D] = -INFINITY;
+        ws_part[(size_t)r * C::PARTIAL_STRIDE + D + 1] = 0.f;
       }
     }
     return;
@@ -223,10 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = b * a.H + h;
     mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      tma_load_3d(sQ + x * kTileBytes, &qmap, 0, q0 + x * kTileM, bh, q_full);
-      tma_load_3d(sQ + x * kTileBytes + kSlabBytes, &qmap, 64, q0 + x * kTileM, bh, q_full);
-    }
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int hf = 0; hf < C::HALVES; ++hf)
+        tma_load_3d(sQ + x * kPTileBytes + hf * kSlabBytes, &qmap, 64 * hf, q0 + x * kTileM,
+                    bh, q_full);
   }
   // The producer's first block-table window, in flight across the sync.
   constexpr int kPerLane = kTblWindow / 32;
@@ -248,12 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
   bool ok = true;
-  int issued = 0;  // K/V tiles the producer issued into the ring
+  int issued = 0;  // K/V tiles the producer issued into the ring by TMA
 
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ producer
     int win = -kTblWindow;
-    if (lane == 0) {
+    if (lane == 0 && !kGatherCp) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
     }
@@ -275,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kPerLane; ++k) {
             const int lb = win + lane + 32 * k;
             ent[k] = lb < nblk_seq ? __ldg(a.block_tables + (size_t)b * a.max_blocks + lb)
-                                   : a.num_blocks;  // past the sequence: TMA fills zeros
+                                   : a.num_blocks;  // past the sequence: zeros
           }
         }
 #pragma unroll
@@ -293,25 +334,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = u % kStages;
       if (lane == 0) {
         ok = mbar_wait(&kv_empty[st], ((u / kStages) & 1) ^ 1);
-        if (ok) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
+        if (ok && !kGatherCp) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
       }
       ok = __shfl_sync(kFull, ok, 0);
-      // One box per lane and block: (64 dims, 8 keys, 2 halves, BS/8 key
-      // groups) at row phys*BS*H + h of the pool seen as [slot*H + head] rows;
-      // past-the-sequence blocks (phys = num_blocks) fall outside the map and
-      // read as zeros.
-      if (ok && lane < BPT) {
-        uint8_t* dst = sKV + st * kTileBytes + lane * (BS / 8) * kGroupBytes;
-        tma_load_5d(dst, v ? &vmap : &kmap, 0, 0, 0, 0, tbl_s[lb0 - win + lane] * BS * a.H + h,
-                    &kv_full[st]);
+      if constexpr (!kGatherCp) {
+        // One box per lane and block: (64 dims, 8 keys, D/64 halves, BS/8 key
+        // groups) at row phys*BS*H + h of the pool seen as [slot*H + head]
+        // rows; past-the-sequence blocks (phys = num_blocks) fall outside the
+        // map and read as zeros.
+        if (ok && lane < BPT) {
+          uint8_t* dst = sKV + st * kTileBytes + lane * (BS / 8) * kGroupBytes;
+          tma_load_5d(dst, v ? &vmap : &kmap, 0, 0, 0, 0,
+                      tbl_s[lb0 - win + lane] * BS * a.H + h, &kv_full[st]);
+        }
+        if (ok && lane == 0) ++issued;
+      } else if (ok) {
+        // Blocks of fewer than 8 tokens: 16-byte copies by the lanes, placed
+        // as the TMA boxes would land them (key r at row r & 7 of group
+        // r >> 3, chunk c of a 64-dim half at c ^ (r & 7)).  Keys of blocks
+        // past the sequence are zero-filled.  Lane l takes keys l + 32 i.
+        const __half* pool = v ? a.v_cache : a.k_cache;
+        uint8_t* tile = sKV + st * kTileBytes;
+#pragma unroll
+        for (int i = 0; i < kTileN / 32; ++i) {
+          const int r = lane + 32 * i;
+          const int phys = tbl_s[lb0 - win + r / BS];
+          uint8_t* grp = tile + (r >> 3) * kGroupBytes + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {  // 16-byte chunks of the row
+            uint8_t* dst = grp + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) * 16);
+            if (phys < a.num_blocks)
+              cp_async16(dst, pool + (((size_t)phys * BS + r % BS) * a.H + h) * D + c * 8);
+            else
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        cp_async_commit();
       }
-      if (ok && lane == 0) ++issued;
+    };
+    // cp.async gathers: tile u is published one load later, once this lane's
+    // copies of it have completed (the group of tile u+1 may still fly); the
+    // proxy fence makes the copied bytes visible to the tensor core.
+    auto publish = [&](int u) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kv_full[u % kStages]);
     };
     int u = 0;
     if (n_kv > 0) load_tile(0, 0, u++);
     for (int j = 0; j < n_kv && ok; ++j) {
-      if (j + 1 < n_kv) load_tile(j + 1, 0, u++);
-      if (ok) load_tile(j, 1, u++);
+      if (j + 1 < n_kv) {
+        load_tile(j + 1, 0, u++);
+        if constexpr (kGatherCp) {
+          if (ok) {
+            cp_async_wait<1>();
+            publish(u - 2);
+          }
+        }
+      }
+      if (ok) {
+        load_tile(j, 1, u++);
+        if constexpr (kGatherCp) {
+          if (ok) {
+            cp_async_wait<1>();
+            publish(u - 2);
+          }
+        }
+      }
+    }
+    if constexpr (kGatherCp) {
+      cp_async_wait<0>();  // none of this warp's copies stays in flight
+      if (ok && u > 0) publish(u - 1);
     }
   } else if (warp == kWarpMma || warp == kWarpPv) {
     // ------------------------------------------------------------ MMA issuers
@@ -336,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (last_x >= 0 && !(ok = mbar_wait(&s_free[last_x], last_t & 1))) break;
             if (!(ok = landed(u))) break;
             tc::fence_after_sync();
-            const uint64_t db = dk + (u % kStages) * kTileDesc;
-            const uint32_t ta = tmem + kColQ + x * (kD / 2);
+            const uint64_t db = dk + (u % kStages) * C::TILE_DESC;
+            const uint32_t ta = tmem + kColQ + x * (D / 2);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              tc::mma_f16_ts(tmem + kColS, ta + kk * 8, db + kgroup_off(kk), kIdescS, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc::mma_f16_ts(tmem + kColS, ta + kk * 8, db + kgroup_off(kk), C::IDESC_S, kk > 0);
             tc::commit(&s_full[x]);
             s_issued[x] = t + 1;  // read by the P V issuer (a scheduling hint only)
             last_x = x;
@@ -367,12 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chain does not depend on this product, so the wait ends.
           if (t + 1 < nt[x] && !(ok = wait_issued(s_issued + x, t + 2))) break;
           tc::fence_after_sync();
-          const uint64_t da = dp + x * kTileDesc;
-          const uint64_t db = dv + (u % kStages) * kTileDesc;
+          const uint64_t da = dp + x * kPTileDesc;
+          const uint64_t db = dv + (u % kStages) * C::TILE_DESC;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            tc::mma_f16(tmem + kColO + x * kD, da + kmajor_off(kk), db + vmn_off(kk), kIdescO,
-                        (t > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16(tmem + kColO + x * D, da + kmajor_off(kk), db + vmn_off<D>(kk),
+                        C::IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&pv_done[x]);
         }
         if (ok) tc::commit(&kv_empty[u % kStages]);  // V_t has no further reader
@@ -387,8 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(kFull, ok, 0);
           if (ok) {
             uint8_t* vt = sKV + (u % kStages) * kTileBytes;
-            for (int i = lane; i < (kTileN - tail_rows) * 16; i += 32) {  // 16 chunks per row
-              const int r = tail_rows + (i >> 4), c = i & 15;
+            constexpr int kChunks = D / 8;  // 16-byte chunks per row
+            for (int i = lane; i < (kTileN - tail_rows) * kChunks; i += 32) {
+              const int r = tail_rows + i / kChunks, c = i % kChunks;
               *reinterpret_cast<uint4*>(vt + (r >> 3) * kGroupBytes + (c >> 3) * 1024 +
                                         (r & 7) * 128 + (c & 7) * 16) =
                   make_uint4(0u, 0u, 0u, 0u);
@@ -408,19 +502,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_s = tmem + t_lane + kColS;
-    const uint32_t t_o = tmem + t_lane + kColO + x * kD;
+    const uint32_t t_o = tmem + t_lane + kColO + x * D;
     const int pos0 = x ? pos0_b : pos0_a;
     const int pos = pos0 + row;
     const int ntile = x ? ntile_b : ntile_a;
     const float sl2 = a.scale_log2;
-    uint8_t* prow = sP + x * kTileBytes + row * 128;
+    uint8_t* prow = sP + x * kPTileBytes + row * 128;
     float m = -INFINITY, l = 0.f;
     // Q row (staged by TMA in the P tile, 128-byte swizzle) into tensor
     // memory: column c of Q_X holds dims 2c, 2c+1.
     ok = __all_sync(kFull, mbar_wait(q_full, 0));
     if (ok) {
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int hf = 0; hf < C::HALVES; ++hf) {
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -431,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[4 * c + 2] = v.z;
           w[4 * c + 3] = v.w;
         }
-        tc::st_32x32(tmem + t_lane + kColQ + x * (kD / 2) + hf * 32, w);
+        tc::st_32x32(tmem + t_lane + kColQ + x * (D / 2) + hf * 32, w);
       }
       tc::wait_st();
       tc::fence_before_sync();
@@ -504,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j > 0 && __any_sync(kFull, resc)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tc::ld_32x32(t_o + c * 32, o);
           tc::wait_ld();
@@ -537,10 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && part >= 0) {
       // Part of a split unit: the unnormalised row (o, m, l) for the combine;
       // a Q tile with no key tile in this part leaves an empty partial.
-      float* wrow = ws_part + (size_t)(x * kTileM + row) * kPrefillPartialStride;
+      float* wrow = ws_part + (size_t)(x * kTileM + row) * C::PARTIAL_STRIDE;
       if (ntile > 0) tc::fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         if (ntile > 0) {
           tc::ld_32x32(t_o + c * 32, o);
@@ -555,18 +649,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
       }
-      wrow[kD] = ntile > 0 ? m : -INFINITY;
-      wrow[kD + 1] = ntile > 0 ? l : 0.f;
+      wrow[D] = ntile > 0 ? m : -INFINITY;
+      wrow[D + 1] = ntile > 0 ? l : 0.f;
     } else if (ok && ntile > 0) {
       // The output tile goes through the P tile (free: every P V product of X
-      // is done), swizzled like the TMA tiles, and leaves by two TMA stores:
-      // one 16 KB copy per 64-dim half instead of 16 scattered 16-byte stores
-      // per thread.  Rows past the chunk fall outside the tensor map and are
-      // not written.
+      // is done), swizzled like the TMA tiles, and leaves by TMA stores: one
+      // 16 KB copy per 64-dim half instead of scattered 16-byte stores per
+      // thread.  Rows past the chunk fall outside the tensor map and are not
+      // written.
       tc::fence_after_sync();
       const float inv = 1.f / l;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // dims 32c .. 32c+31
+      for (int c = 0; c < D / 32; ++c) {  // dims 32c .. 32c+31
         uint32_t o[32];
         tc::ld_32x32(t_o + c * 32, o);
         tc::wait_ld();
@@ -589,8 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1 + x, 128);
       if (quarter == 0 && lane == 0) {
         const int bh = b * a.H + h;
-        tma_store_3d(&omap, sP + x * kTileBytes, 0, q0 + x * kTileM, bh);
-        tma_store_3d(&omap, sP + x * kTileBytes + kSlabBytes, 64, q0 + x * kTileM, bh);
+#pragma unroll
+        for (int hf = 0; hf < C::HALVES; ++hf)
+          tma_store_3d(&omap, sP + x * kPTileBytes + hf * kSlabBytes, 64 * hf, q0 + x * kTileM,
+                       bh);
         bulk_commit_group();
         bulk_wait_all();  // the shared-memory source stays valid until the CTA exits
       }
@@ -621,9 +717,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge the parts of split units by log-sum-exp (m, l in the softmax's log2
-// domain): one warp per query row, lane l owns dims [4l, 4l + 4).
+// domain): one warp per query row, lane l owns dims [l * D/32, (l+1) * D/32).
+template <int D>
 __global__ void __launch_bounds__(256)
     prefill_combine_kernel(const PrefillArgs a, int n_split_units) {
+  constexpr int EPL = D / 32;
+  constexpr int kStride = PfCfg<D>::PARTIAL_STRIDE;
   pdl_wait();  // the partials come from the prefill kernel just before
   const int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -633,46 +732,60 @@ __global__ void __launch_bounds__(256)
   const int ct = unit % a.gx, h = (unit / a.gx) % a.H, b = unit / (a.gx * a.H);
   const int qi = ct * 2 * kTileM + r;
   if (qi >= a.Lq) return;
-  const float* base = a.ws + (size_t)su * a.split * (2 * kTileM) * kPrefillPartialStride +
-                      (size_t)r * kPrefillPartialStride;
-  const size_t part_stride = (size_t)(2 * kTileM) * kPrefillPartialStride;
+  const float* base = a.ws + (size_t)su * a.split * (2 * kTileM) * kStride + (size_t)r * kStride;
+  const size_t part_stride = (size_t)(2 * kTileM) * kStride;
   // All parts' loads issued together (split <= PK_PREFILL_MAX_SPLIT <= 8).
   constexpr int kMaxParts = 8;
   float ms[kMaxParts], ls[kMaxParts];
-  float4 ov[kMaxParts];
+  float ov[kMaxParts][EPL];
 #pragma unroll
   for (int s = 0; s < kMaxParts; ++s) {
     if (s < a.split) {
       const float* pr = base + s * part_stride;
-      ms[s] = pr[kD];
-      ls[s] = pr[kD + 1];
-      ov[s] = *reinterpret_cast<const float4*>(pr + lane * 4);
+      ms[s] = pr[D];
+      ls[s] = pr[D + 1];
+      if constexpr (EPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(pr + lane * 4);
+        ov[s][0] = t.x; ov[s][1] = t.y; ov[s][2] = t.z; ov[s][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(pr + lane * 2);
+        ov[s][0] = t.x; ov[s][1] = t.y;
+      }
     } else {
       ms[s] = -INFINITY;
       ls[s] = 0.f;
-      ov[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) ov[s][e] = 0.f;
     }
   }
   float M = -INFINITY;
 #pragma unroll
   for (int s = 0; s < kMaxParts; ++s)
     if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
-  float L = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+  float L = 0.f, o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = 0.f;
 #pragma unroll
   for (int s = 0; s < kMaxParts; ++s) {
     if (ls[s] > 0.f) {  // an empty part's o is never read as a number
       const float wgt = ex2_approx(ms[s] - M);
       L += ls[s] * wgt;
-      o[0] += wgt * ov[s].x; o[1] += wgt * ov[s].y; o[2] += wgt * ov[s].z; o[3] += wgt * ov[s].w;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[e] += wgt * ov[s][e];
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  __half2 h0 = __floats2half2_rn(o[0] * inv, o[1] * inv);
-  __half2 h1 = __floats2half2_rn(o[2] * inv, o[3] * inv);
-  uint2 u;
-  u.x = *reinterpret_cast<uint32_t*>(&h0);
-  u.y = *reinterpret_cast<uint32_t*>(&h1);
-  *reinterpret_cast<uint2*>(a.out + (((size_t)b * a.H + h) * a.Lq + qi) * kD + lane * 4) = u;
+  __half* dst = a.out + (((size_t)b * a.H + h) * a.Lq + qi) * D + lane * EPL;
+  if constexpr (EPL == 4) {
+    __half2 h0 = __floats2half2_rn(o[0] * inv, o[1] * inv);
+    __half2 h1 = __floats2half2_rn(o[2] * inv, o[3] * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+    *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(o[0] * inv, o[1] * inv);
+  }
 }
 
 #ifndef PK_PREFILL_MAX_SPLIT
@@ -701,14 +814,17 @@ SplitPlan split_plan(int B, int H, int Lq) {
   return p;
 }
 
-template <int BS>
+template <int D, int BS>
 cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const void* v_cache,
                              cudaStream_t stream) {
+  using C = PfCfg<D>;
   PrefillArgs a = a_in;
+  a.k_cache = reinterpret_cast<const __half*>(k_cache);
+  a.v_cache = reinterpret_cast<const __half*>(v_cache);
   a.gx = (a.Lq + 2 * kTileM - 1) / (2 * kTileM);
   SplitPlan plan = split_plan(a.B, a.H, a.Lq);
   const size_t need = (size_t)(plan.units - plan.full_units) * plan.split * (2 * kTileM) *
-                      kPrefillPartialStride;
+                      C::PARTIAL_STRIDE;
   if (plan.split > 1 && (a.ws == nullptr || a.ws_floats < need)) {
     plan.full_units = plan.units;  // no workspace: every unit whole
     plan.split = 1;
@@ -719,36 +835,39 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
   const long long rows = (long long)a.num_blocks * BS;
   cudaError_t e;
   {
-    unsigned long long dims[3] = {(unsigned long long)kD, (unsigned long long)a.Lq,
+    unsigned long long dims[3] = {(unsigned long long)D, (unsigned long long)a.Lq,
                                   (unsigned long long)a.B * a.H};
-    unsigned long long strides[2] = {(unsigned long long)kD * 2,
-                                     (unsigned long long)a.Lq * kD * 2};
+    unsigned long long strides[2] = {(unsigned long long)D * 2,
+                                     (unsigned long long)a.Lq * D * 2};
     unsigned box[3] = {64, kTileM, 1};
     e = make_map_3d(&qmap, a.q, dims, strides, box, true);
     if (e != cudaSuccess) return e;
     e = make_map_3d(&omap, a.out, dims, strides, box, true);  // same layout as q
     if (e != cudaSuccess) return e;
   }
-  {
-    // The pool as rows r = slot * H + head of 128 fp16, and inside a block
+  memset(&kmap, 0, sizeof(kmap));  // unused by the cp.async gather of 4-token blocks
+  memset(&vmap, 0, sizeof(vmap));
+  if constexpr (BS >= 8) {
+    // The pool as rows r = slot * H + head of D fp16, and inside a block
     // (rows r, r + H, ..., r + (BS-1) H from its first slot) the box order
-    // (64 dims, 8 keys, 2 halves, BS/8 key groups).
-    const unsigned long long row = (unsigned long long)kD * 2, tok = row * a.H;
-    unsigned long long dims[5] = {64, 8, 2, BS / 8, (unsigned long long)rows * a.H};
+    // (64 dims, 8 keys, D/64 halves, BS/8 key groups).
+    const unsigned long long row = (unsigned long long)D * 2, tok = row * a.H;
+    unsigned long long dims[5] = {64, 8, (unsigned long long)C::HALVES,
+                                  (unsigned long long)BS / 8, (unsigned long long)rows * a.H};
     unsigned long long strides[4] = {tok, 128, 8 * tok, row};
-    unsigned box[5] = {64, 8, 2, BS / 8, 1};
+    unsigned box[5] = {64, 8, (unsigned)C::HALVES, (unsigned)BS / 8, 1};
     e = make_map_5d(&kmap, k_cache, dims, strides, box, true);
     if (e != cudaSuccess) return e;
     e = make_map_5d(&vmap, v_cache, dims, strides, box, true);
     if (e != cudaSuccess) return e;
   }
-  constexpr auto kern = prefill_kernel<BS>;
-  e = ensure_dynamic_smem<kern>(kSmemBytes);
+  constexpr auto kern = prefill_kernel<D, BS>;
+  e = ensure_dynamic_smem<kern>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.full_units + (plan.units - plan.full_units) * plan.split);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -764,27 +883,30 @@ cudaError_t launch_prefill_t(const PrefillArgs& a_in, const void* k_cache, const
   cc.stream = stream;
   cc.attrs = attr;
   cc.numAttrs = 1;
-  return cudaLaunchKernelEx(&cc, prefill_combine_kernel, a, n_split);
+  return cudaLaunchKernelEx(&cc, prefill_combine_kernel<D>, a, n_split);
 }
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int B, int H, int Lq) {
-  if (B <= 0 || H <= 0 || Lq <= 0) return 0;
+size_t prefill_workspace_bytes(int B, int H, int Lq, int D) {
+  if (B <= 0 || H <= 0 || Lq <= 0 || (D != 64 && D != 128)) return 0;
   const SplitPlan p = split_plan(B, H, Lq);
-  return (size_t)(p.units - p.full_units) * p.split * (2 * kTileM) * kPrefillPartialStride *
-         sizeof(float);
+  return (size_t)(p.units - p.full_units) * p.split * (2 * kTileM) * (D + 4) * sizeof(float);
 }
 
 bool prefill_supported(int D, int block_size) {
-  return D == kD && (block_size == 16 || block_size == 32);
+  return (D == 64 || D == 128) &&
+         (block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                            cudaStream_t stream) {
   if (a.H > 65535 || a.B > 65535) return cudaErrorInvalidValue;
-  if (a.block_size == 16) return launch_prefill_t<16>(a, k_cache, v_cache, stream);
-  if (a.block_size == 32) return launch_prefill_t<32>(a, k_cache, v_cache, stream);
+#define PK_PF_CASE(DD, BB) \
+  if (a.D == DD && a.block_size == BB) return launch_prefill_t<DD, BB>(a, k_cache, v_cache, stream);
+  PK_PF_CASE(128, 16) PK_PF_CASE(128, 32) PK_PF_CASE(128, 8) PK_PF_CASE(128, 4)
+  PK_PF_CASE(64, 16) PK_PF_CASE(64, 32) PK_PF_CASE(64, 8) PK_PF_CASE(64, 4)
+#undef PK_PF_CASE
   return cudaErrorInvalidValue;
 }
 

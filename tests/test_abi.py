@@ -126,9 +126,10 @@ def test_copy_validation(lib):
 
 
 def test_prefill_validation(lib):
-    rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 64, 4, 8, 4,
-                              0.1, 0x1000, NULL, 0, NULL, NULL)
-    assert rc == pk.PA_ERR_UNSUPPORTED  # (D=64, bs=4) has no tensor-core kernel
+    for D, bs in ((96, 16), (256, 16), (128, 12), (64, 64)):  # no kernel for these
+        rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, D, bs, 8, 4,
+                                  0.1, 0x1000, NULL, 0, NULL, NULL)
+        assert rc == pk.PA_ERR_UNSUPPORTED, (D, bs)
     rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, -2, 4, 8, 128, 16, 8, 4,
                               0.1, 0x1000, NULL, 0, NULL, NULL)
     assert rc == pk.PA_ERR_INVALID

@@ -29,8 +29,8 @@ def run_prefill(g, scale, status=None, out=None):
                                g["context_lens"], scale, status=status, out=out)
 
 
-def check_against_oracle(B, H, bs, Lq, ctx, seed, what):
-    batch = workloads.random_prefill(B, H, 128, bs, Lq, ctx, seed=seed, device="cpu",
+def check_against_oracle(B, H, bs, Lq, ctx, seed, what, D=128):
+    batch = workloads.random_prefill(B, H, D, bs, Lq, ctx, seed=seed, device="cpu",
                                      write_chunk=False)
     ref = oracle.prefill(batch.q.numpy(), batch.k_cache.numpy(), batch.v_cache.numpy(),
                          batch.block_tables.numpy(), batch.context_lens.numpy(), batch.scale)
@@ -55,6 +55,52 @@ def test_prefill_two_key_tiles():
                                     (256, [1000, 700]), (37, [4096, 37])])
 def test_prefill_ragged(bs, Lq, ctx):
     check_against_oracle(len(ctx), 3, bs, Lq, ctx, seed=42 + Lq, what=f"bs={bs} Lq={Lq} {ctx}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [4, 8, 16, 32])
+@pytest.mark.parametrize("Lq,ctx", [(1, [1, 77]), (100, [100, 300]), (200, [333, 200]),
+                                    (257, [257, 900]), (37, [1500, 37])])
+def test_prefill_head_dims_and_block_sizes(D, bs, Lq, ctx):
+    """Every (head_dim, block_size) the library takes: 64-dim rows (one
+    swizzle half) and 4-token blocks (gathered by cp.async, two blocks per
+    8-row swizzle atom) included, ragged chunks and contexts."""
+    check_against_oracle(len(ctx), 3, bs, Lq, ctx, seed=70 + Lq + bs + D, D=D,
+                         what=f"D={D} bs={bs} Lq={Lq} {ctx}")
+
+
+@pytest.mark.parametrize("D,bs", [(64, 16), (64, 4), (128, 4), (128, 8)])
+def test_prefill_permutation_invariance_small_blocks_and_d64(D, bs):
+    batch = workloads.random_prefill(2, 3, D, bs, 160, [600, 300], seed=53 + bs + D,
+                                     device="cpu", write_chunk=False)
+    g = to_dev(batch, DEV)
+    out = run_prefill(g, batch.scale)
+    perm = torch.randperm(batch.num_blocks, generator=torch.Generator().manual_seed(6))
+    k2 = torch.empty_like(batch.k_cache)
+    v2 = torch.empty_like(batch.v_cache)
+    k2[perm] = batch.k_cache
+    v2[perm] = batch.v_cache
+    bt = batch.block_tables.long()
+    t2 = torch.where(bt >= 0, perm[bt.clamp(min=0)], torch.full_like(bt, -1)).int()
+    out2 = run_prefill(dict(g, k_cache=k2.to(DEV), v_cache=v2.to(DEV),
+                            block_tables=t2.to(DEV)), batch.scale)
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("D,bs", [(64, 16), (64, 4), (128, 4)])
+def test_prefill_value_ones_and_bad_block_small_blocks_and_d64(D, bs):
+    batch = workloads.random_prefill(2, 2, D, bs, 130, [500, 130], seed=54 + bs + D,
+                                     device=DEV, write_chunk=False)
+    g = to_dev(batch, DEV)
+    out = run_prefill(dict(g, v_cache=torch.ones_like(g["v_cache"])), batch.scale)
+    assert torch.all(out == 1.0)
+    # a block id past the pool: flagged, never dereferenced (read as zeros)
+    bt = g["block_tables"].clone()
+    bt[0, 3] = batch.num_blocks + 5
+    status = zero_status(DEV)
+    run_prefill(dict(g, block_tables=bt), batch.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pk.PA_DEV_BAD_BLOCK_ID
 
 
 def test_prefill_lq1_matches_decode():
@@ -177,6 +223,34 @@ def test_prefill_long_chunks_ragged(bs, Lq, ctx):
     ragged inside either of its two Q tiles."""
     check_against_oracle(len(ctx), 2, bs, Lq, ctx, seed=60 + Lq + bs,
                          what=f"long chunk bs={bs} Lq={Lq} {ctx}")
+
+
+@pytest.mark.parametrize("D,bs", [(64, 16), (64, 8), (128, 4)])
+def test_tail_split_d64_and_small_blocks(D, bs):
+    # As above for 64-dim heads (the combine's two dims per lane) and for the
+    # cp.async gather: H = SMs + 8 heads, one unit per head, the last 8 split.
+    nsm = torch.cuda.get_device_properties(DEV).multi_processor_count
+    H, Lq = nsm + 8, 256
+    ctx = [Lq + 3 * 128 + 21]
+    assert pk.pa_prefill_workspace_size(1, H, Lq, D) > 0
+    batch = workloads.random_prefill(1, H, D, bs, Lq, ctx, seed=97 + D + bs, device="cpu",
+                                     write_chunk=False)
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out_split = run_prefill(g, batch.scale, status=status)
+    out_whole = pk.pa_prefill_chunk(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                    g["context_lens"], batch.scale, tail_split=False,
+                                    status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    hs = list(range(H - 10, H))
+    sl = lambda t: t[:, :, hs].contiguous()
+    ref = oracle.prefill(batch.q[:, hs].contiguous().numpy(), sl(batch.k_cache).numpy(),
+                         sl(batch.v_cache).numpy(), batch.block_tables.numpy(),
+                         batch.context_lens.numpy(), batch.scale)
+    assert_close(out_split[:, hs], ref, what=f"tail-split heads D={D} bs={bs}")
+    e = errors(out_split, out_whole.float().cpu().numpy().astype(np.float64))
+    assert e[0] <= 2e-3, e
 
 
 def test_tail_split_two_units_per_head():

@@ -43,10 +43,10 @@ def poison(batch):
 
 
 @pytest.mark.parametrize("Lq", [200, 400])  # one and two work units per (sequence, head)
-@pytest.mark.parametrize("bs", [16, 32])
-def test_prefill_ignores_stale_slots(bs, Lq):
+@pytest.mark.parametrize("bs,D", [(16, 128), (32, 128), (4, 128), (8, 64), (4, 64)])
+def test_prefill_ignores_stale_slots(bs, Lq, D):
     ctx = [Lq + 333, Lq + 1007, Lq + 9]  # partial last blocks
-    batch = workloads.random_prefill(len(ctx), 3, 128, bs, Lq, ctx, seed=300 + bs + Lq,
+    batch = workloads.random_prefill(len(ctx), 3, D, bs, Lq, ctx, seed=300 + bs + Lq + D,
                                      device="cpu", write_chunk=False)
     n_unused, n_tails = poison(batch)
     assert n_tails == len(ctx)
@@ -59,7 +59,7 @@ def test_prefill_ignores_stale_slots(bs, Lq):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert torch.isfinite(out).all()
-    assert_close(out, ref, what=f"prefill with NaN in unread slots bs={bs} Lq={Lq}")
+    assert_close(out, ref, what=f"prefill with NaN in unread slots bs={bs} D={D} Lq={Lq}")
 
 
 @pytest.mark.parametrize("bs", [4, 16, 32])
