@@ -22,21 +22,23 @@
 //   warp 10     P V issuer (one thread).
 // Head dims 128 and 64 are instantiations of the same kernel (D / 64 halves
 // of 64 dims; 128-byte swizzle rows of 64 fp16).
-// Tensor memory: S [0,128) shared by the two tiles, Q_A and Q_B from column
-// 128 (D/2 columns each, fp16 pairs), O_A and O_B from column 256 (D columns
-// each).  Q sits in tensor memory (S = Q K^T takes its A operand from there)
-// so that shared memory holds a deep K/V ring: with Q in shared memory only
-// 3 slots of 32 KB fit and K/V tiles landed late.  Q arrives by TMA in the P
-// buffers, which are free until the first P store; each softmax thread moves
-// its row into tensor memory.
+// Tensor memory: S [0,128) shared by the two tiles, P_A [128,192) and P_B
+// [192,256) (fp16 pairs: column c holds keys 2c, 2c+1), O_A and O_B from
+// column 256 (D columns each).  Q stays in shared memory where TMA put it
+// (the A operand of S = Q K^T) and P lives in tensor memory (the A operand
+// of O += P V): per key tile the shared memory then serves 64 KB of TMA
+// fills, Q and K reads of the two S products and the V reads of the two
+// P V products (~256 KB) where P in shared memory cost another 64 KB of P
+// stores and 64 KB of P reads (~320 KB); its bandwidth, not the tensor pipe,
+// bounded that layout.
 // Softmax of tile X, key tile j: wait for S_X(j), load the whole row into
 // registers and release S at once, so the tensor core computes the other
 // tile's S while this softmax still works on j.  Row max (keys past the row's position
 // skipped on diagonal tiles); p = 2^(s*scale*log2e - m) (one FMA, one ex2)
 // packed to fp16 in registers with the row sum; then wait for P_X(j-1) V_{j-1}
-// (so O_X is stable and the P_X tile free), rescale O_X only when the row max
-// grew by more than 2^8 (P then stays <= 256, exact in fp16 range), store P_X
-// to shared memory.
+// (so O_X is stable and P_X free), rescale O_X only when the row max grew by
+// more than 2^8 (P then stays <= 256, exact in fp16 range), store P_X to
+// tensor memory (two 32-column stores).
 // The S products go A(0), B(0), A(1), B(1), ..., each once the softmax
 // released the previous one and its K tile landed; O_X += P_X(j) V_j once
 // P_X(j) is stored and V_j landed.  The two
@@ -44,8 +46,9 @@
 // queues behind S products at the issuing end.
 // Operand layouts (tcgen05 shared-memory descriptors, 128-byte swizzle; the
 // 16-byte chunk c of a 128-byte row r sits at chunk position c ^ (r mod 8)):
-//   Q (staged), P: K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B
-//                 apart, 64-element halves 16 KB apart;
+//   Q_X         : K-major, rows of 64 fp16 (128 B), 8-row atoms 1024 B
+//                 apart, 64-element halves 16 KB apart (the TMA boxes'
+//                 landing order; the output tile is staged the same way);
 //   K_j, V_j    : key groups of 8 keys x D dims (D * 16 bytes apart), each
 //                 holding the 1 KB atom of dims 0-63 then (D = 128) that of
 //                 dims 64-127 (the order one box of a block lands in).  K_j
@@ -68,8 +71,8 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTileM = 128;                  // queries per Q tile (two per CTA)
 constexpr int kTileN = 128;                  // keys per tile
-constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16 (a P or staged-Q half)
-constexpr int kPTileBytes = 2 * kSlabBytes;  // P: 128 queries x 128 keys fp16
+constexpr int kSlabBytes = 128 * 128;        // 128 rows x 64 fp16 (half of a Q tile)
+constexpr int kQTileBytes = 2 * kSlabBytes;  // a Q tile's room: 128 queries x up to 128 dims
 constexpr int kThreads = 352;                // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                  // S = Q K^T issuer, tensor-memory owner
@@ -77,13 +80,13 @@ constexpr int kWarpPv = 10;                  // O += P V issuer
 constexpr int kTblWindow = 256;              // block-table entries staged in smem
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColQ = 128;              // Q_A, then Q_B D/2 columns later
+constexpr uint32_t kColP = 128;              // P_A, then P_B 64 columns later
 constexpr uint32_t kColO = 256;              // O_A, then O_B D columns later
 constexpr int kMaxStages = 8;
-constexpr int kNumBars = 1 + 2 * kMaxStages + 2 + 2 + 2 + 2 + 1 + 2;
+constexpr int kNumBars = 1 + 2 * kMaxStages + 2 + 2 + 2 + 2 + 1;
 
 // Per head dim: the K/V tile (128 keys x D dims), its 8-key groups, and the
-// ring depth that fills the shared memory the two P tiles leave.
+// ring depth that fills the shared memory the two Q tiles leave.
 template <int D>
 struct PfCfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
@@ -92,8 +95,8 @@ struct PfCfg {
   static constexpr int GROUP_BYTES = 8 * D * 2;         // 8 keys x D dims
   static constexpr int STAGES = D == 128 ? 5 : 8;       // K/V ring slots
   static_assert(STAGES <= kMaxStages, "barrier room");
-  static constexpr int OFF_P = 0;                       // P_A, P_B (Q staged first)
-  static constexpr int OFF_KV = OFF_P + 2 * kPTileBytes;
+  static constexpr int OFF_Q = 0;                       // Q_A, Q_B (then the output tiles)
+  static constexpr int OFF_KV = OFF_Q + 2 * kQTileBytes;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
   static constexpr int OFF_TMEM_HOLDER = OFF_BAR + kNumBars * 8;
   static constexpr int OFF_ISSUED = OFF_TMEM_HOLDER + 4;  // [2] S products issued per tile
@@ -106,10 +109,10 @@ struct PfCfg {
   static constexpr int PARTIAL_STRIDE = D + 4;            // o[D], m, l, pad (16-byte rows)
 };
 
-constexpr uint32_t kPTileDesc = kPTileBytes >> 4;  // one P tile, descriptor units
+constexpr uint32_t kQTileDesc = kQTileBytes >> 4;  // one Q tile, descriptor units
 
 // Descriptor address offset of K step kk (16 elements = 32 B) of a K-major
-// P tile: inside the 64-element half kk / 4.
+// Q tile: inside the 64-element half kk / 4.
 __device__ __forceinline__ constexpr uint32_t kmajor_off(int kk) {
   return (uint32_t)((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
 }
@@ -170,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
-  uint8_t* sQ = smem + C::OFF_P;  // staging only
-  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sQ = smem + C::OFF_Q;  // Q_A, Q_B; each becomes its tile's output staging
   uint8_t* sKV = smem + C::OFF_KV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
@@ -182,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_free + 2;          // [2]: P_X(j) stored
   uint64_t* pv_done = p_full + 2;         // [2]: O_X += P_X(j) V_j completed
   uint64_t* drain = pv_done + 2;
-  uint64_t* q_ready = drain + 1;          // [2]: Q_X moved into tensor memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_HOLDER);
   int32_t* tbl_s = reinterpret_cast<int32_t*>(smem + C::OFF_TBL);
   volatile int* s_issued = reinterpret_cast<volatile int*>(smem + C::OFF_ISSUED);
@@ -254,19 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_free[i], 4);  // one arrival per softmax warp
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&q_ready[i], 4);
     }
     mbar_init(drain, 2);
     fence_mbar_init();
     // Q goes out first, before tensor memory is allocated and the CTA syncs:
-    // it heads the start-up path (Q -> tensor memory -> first S product).
+    // it heads the start-up path (Q -> first S product).
     const int bh = b * a.H + h;
     mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
 #pragma unroll
     for (int x = 0; x < 2; ++x)
 #pragma unroll
       for (int hf = 0; hf < C::HALVES; ++hf)
-        tma_load_3d(sQ + x * kPTileBytes + hf * kSlabBytes, &qmap, 64 * hf, q0 + x * kTileM,
+        tma_load_3d(sQ + x * kQTileBytes + hf * kSlabBytes, &qmap, 64 * hf, q0 + x * kTileM,
                     bh, q_full);
   }
   // The producer's first block-table window, in flight across the sync.
@@ -419,21 +419,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Base descriptors; each MMA adds a compile-time offset (a slot, a
         // tile or a K step never carries out of the 14-bit address field).
         const uint64_t dk = tc::smem_desc(smem_u32(sKV), 16, kGroupBytes, tc::kSwizzle128B);
+        const uint64_t dq = tc::smem_desc(smem_u32(sQ), 16, 1024, tc::kSwizzle128B);
+        bool q_landed = false;
         int last_x = -1, last_t = 0;  // the S product issued last
         for (int t = 0; t < n_kv && ok; ++t) {
           const int u = load_k(t);
           for (int x = 0; x < 2 && ok; ++x) {
             if (t >= nt[x]) continue;
-            if (t == 0 && !(ok = mbar_wait(&q_ready[x], 0))) break;
+            if (!q_landed && !(ok = q_landed = mbar_wait(q_full, 0))) break;
             // S is free once the softmax of the previous product loaded it
             if (last_x >= 0 && !(ok = mbar_wait(&s_free[last_x], last_t & 1))) break;
             if (!(ok = landed(u))) break;
             tc::fence_after_sync();
             const uint64_t db = dk + (u % kStages) * C::TILE_DESC;
-            const uint32_t ta = tmem + kColQ + x * (D / 2);
+            const uint64_t da = dq + x * kQTileDesc;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              tc::mma_f16_ts(tmem + kColS, ta + kk * 8, db + kgroup_off(kk), C::IDESC_S, kk > 0);
+              tc::mma_f16(tmem + kColS, da + kmajor_off(kk), db + kgroup_off(kk), C::IDESC_S,
+                          kk > 0 ? 1u : 0u);
             tc::commit(&s_full[x]);
             s_issued[x] = t + 1;  // read by the P V issuer (a scheduling hint only)
             last_x = x;
@@ -443,7 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      const uint64_t dp = tc::smem_desc(smem_u32(sP), 16, 1024, tc::kSwizzle128B);
       const uint64_t dv = tc::smem_desc(smem_u32(sKV), 1024, kGroupBytes, tc::kSwizzle128B);
       // Rows of the last key tile at or past the context length come from the
       // unused tail of the last block (never written: possibly NaN) and would
@@ -460,12 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chain does not depend on this product, so the wait ends.
           if (t + 1 < nt[x] && !(ok = wait_issued(s_issued + x, t + 2))) break;
           tc::fence_after_sync();
-          const uint64_t da = dp + x * kPTileDesc;
+          const uint32_t ta = tmem + kColP + x * (kTileN / 2);
           const uint64_t db = dv + (u % kStages) * C::TILE_DESC;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            tc::mma_f16(tmem + kColO + x * D, da + kmajor_off(kk), db + vmn_off<D>(kk),
-                        C::IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16_ts(tmem + kColO + x * D, ta + kk * 8, db + vmn_off<D>(kk), C::IDESC_O,
+                           (t > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&pv_done[x]);
         }
         if (ok) tc::commit(&kv_empty[u % kStages]);  // V_t has no further reader
@@ -507,31 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = pos0 + row;
     const int ntile = x ? ntile_b : ntile_a;
     const float sl2 = a.scale_log2;
-    uint8_t* prow = sP + x * kPTileBytes + row * 128;
+    uint8_t* orow = sQ + x * kQTileBytes + row * 128;  // output staging (Q's room)
     float m = -INFINITY, l = 0.f;
-    // Q row (staged by TMA in the P tile, 128-byte swizzle) into tensor
-    // memory: column c of Q_X holds dims 2c, 2c+1.
+    // Q lands in shared memory by TMA and is read there by the S products;
+    // waiting for it here also keeps a CTA with no S product to issue from
+    // leaving while its copy is in flight.
     ok = __all_sync(kFull, mbar_wait(q_full, 0));
-    if (ok) {
-#pragma unroll
-      for (int hf = 0; hf < C::HALVES; ++hf) {
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(prow + hf * kSlabBytes +
-                                                          ((c ^ (row & 7)) * 16));
-          w[4 * c] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
-        }
-        tc::st_32x32(tmem + t_lane + kColQ + x * (D / 2) + hf * 32, w);
-      }
-      tc::wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_ready[x]);
-    }
     for (int j = 0; j < ntile && ok; ++j) {
       if (!(ok = __all_sync(kFull, mbar_wait(&s_full[x], j & 1)))) break;
       tc::fence_after_sync();
@@ -608,18 +591,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::wait_st();
       }
-      // Store P: 32 keys = four 16-byte chunks, swizzled like the TMA tiles.
+      // Store P into tensor memory: column c of P_X holds keys 2c, 2c+1 (the
+      // A operand of O += P V; chunk c of the row packed in r[c][0..15]).
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint8_t* slab = prow + (c >> 1) * kSlabBytes;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pw[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = (((c & 1) << 2) + q) ^ (row & 7);
-          *reinterpret_cast<uint4*>(slab + chunk * 16) =
-              make_uint4(r[c][4 * q], r[c][4 * q + 1], r[c][4 * q + 2], r[c][4 * q + 3]);
+        for (int e = 0; e < 16; ++e) {
+          pw[e] = r[2 * hf][e];
+          pw[16 + e] = r[2 * hf + 1][e];
         }
+        tc::st_32x32(tmem + t_lane + kColP + x * (kTileN / 2) + hf * 32, pw);
       }
-      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
+      tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[x]);
@@ -652,11 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       wrow[D] = ntile > 0 ? m : -INFINITY;
       wrow[D + 1] = ntile > 0 ? l : 0.f;
     } else if (ok && ntile > 0) {
-      // The output tile goes through the P tile (free: every P V product of X
-      // is done), swizzled like the TMA tiles, and leaves by TMA stores: one
-      // 16 KB copy per 64-dim half instead of scattered 16-byte stores per
-      // thread.  Rows past the chunk fall outside the tensor map and are not
-      // written.
+      // The output tile goes through Q_X's room (free: every S product of X
+      // is done, since its last P V product is), swizzled like the TMA tiles,
+      // and leaves by TMA stores: one 16 KB copy per 64-dim half instead of
+      // scattered 16-byte stores per thread.  Rows past the chunk fall outside
+      // the tensor map and are not written.
       tc::fence_after_sync();
       const float inv = 1.f / l;
 #pragma unroll
@@ -671,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         __uint_as_float(o[2 * i + 1]) * inv);
           hv[i] = *reinterpret_cast<uint32_t*>(&t);
         }
-        uint8_t* slab = prow + (c >> 1) * kSlabBytes;
+        uint8_t* slab = orow + (c >> 1) * kSlabBytes;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int chunk = (((c & 1) << 2) + q) ^ (row & 7);
@@ -685,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bh = b * a.H + h;
 #pragma unroll
         for (int hf = 0; hf < C::HALVES; ++hf)
-          tma_store_3d(&omap, sP + x * kPTileBytes + hf * kSlabBytes, 64 * hf, q0 + x * kTileM,
+          tma_store_3d(&omap, sQ + x * kQTileBytes + hf * kSlabBytes, 64 * hf, q0 + x * kTileM,
                        bh);
         bulk_commit_group();
         bulk_wait_all();  // the shared-memory source stays valid until the CTA exits
