@@ -160,8 +160,10 @@ pa_status pa_decode(const pa_half *q, const pa_half *k_cache,
  * (the first member's table is read for them) and that every member's
  * context holds the prefix.  max_prefix_len bounds group_prefix_len on the
  * host.  Only whole partitions are shared: choose partition_tokens dividing
- * the shared prefix for the full benefit.  D in {64, 128}, block_size in
- * {16, 32}; other sizes return PA_ERR_UNSUPPORTED when num_groups > 0.
+ * the shared prefix for the full benefit; partitions are shared only when
+ * partition_tokens is a multiple of 16 (with other sizes every member reads
+ * its own, same result).  D in {64, 128}, block_size in {4, 8, 16, 32}
+ * (4-token blocks are copied by the lanes, the slower path).
  * ------------------------------------------------------------------------- */
 pa_status pa_decode_shared_prefix(const pa_half *q, const pa_half *k_cache,
                                   const pa_half *v_cache,

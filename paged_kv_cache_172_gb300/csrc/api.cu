@@ -342,7 +342,9 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
                                         (unsigned long long)rows};
     const unsigned long long strides[2] = {(unsigned long long)D * 2,
                                            (unsigned long long)H * D * 2};
-    const unsigned box[3] = {64, 1, 16};
+    // one block's rows per box below 16 tokens (4-token blocks are copied by
+    // the lanes and never use these maps)
+    const unsigned box[3] = {64, 1, (unsigned)(block_size < 16 ? block_size : 16)};
     if (pk::make_map_3d(&maps.ksw, k_cache, dims, strides, box, true) != cudaSuccess ||
         pk::make_map_3d(&maps.vsw, v_cache, dims, strides, box, true) != cudaSuccess)
       return PA_ERR_INVALID;

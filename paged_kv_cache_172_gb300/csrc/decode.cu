@@ -273,12 +273,14 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
   const int tok0 = part * a.part_tokens;
   const size_t row_bh = (size_t)b * a.H + h;
-  if (a.seq_group != nullptr) {  // partitions inside the group's shared prefix
+  // Partitions inside a group's shared prefix (partitions of whole 16-token
+  // stages; with other partition sizes every member computes its own).
+  if (a.seq_group != nullptr && a.part_tokens % pfx::kTB == 0) {
     const int g = a.seq_group[b];
     if (g >= 0 && g < a.num_groups) {
       const int shared = min(a.group_prefix_len[g], ctx) / a.part_tokens * a.part_tokens;
       if (tok0 + a.part_tokens <= shared) {
-        if constexpr (GRP && !FP8 && BS % 16 == 0) {
+        if constexpr (GRP && !FP8) {
           // The group's first member computes this partition for every member.
           if (a.group_seqs[a.group_offsets[g]] == b) {
             const uint32_t sa = smem_u32(smem);
@@ -729,13 +731,13 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
   dim3 grid(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts);
   cudaError_t e;
   bool grouped = false;
-  if constexpr (!FP8 && BS % 16 == 0) grouped = a.seq_group != nullptr;
+  if constexpr (!FP8) grouped = a.seq_group != nullptr;
   if (!grouped) {
     constexpr auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
     e = ensure_dynamic_smem<kern>(Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
-  } else if constexpr (!FP8 && BS % 16 == 0) {
+  } else if constexpr (!FP8) {
     // The grouped grid also runs the shared-prefix partitions.
     constexpr int kPfxSmem = pfx::PrefixCfg<D, T::WARPS>::SMEM;
     constexpr int kSmem = Cfg::SMEM_BYTES > kPfxSmem ? Cfg::SMEM_BYTES : kPfxSmem;
@@ -759,7 +761,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
 }  // namespace
 
 bool prefix_supported(int D, int block_size, int max_group_size) {
-  return (D == 64 || D == 128) && (block_size == 16 || block_size == 32) &&
+  return (D == 64 || D == 128) &&
+         (block_size == 4 || block_size == 8 || block_size == 16 || block_size == 32) &&
          max_group_size >= 1 && max_group_size <= pfx::kMaxMembers;
 }
 

@@ -77,6 +77,20 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 16-byte asynchronous global -> shared copy in the thread's current cp.async
+// group; commit the group; wait until at most N groups are pending.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pfx() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -91,13 +105,20 @@ __device__ __forceinline__ int seq_ctx(const DecodeArgs& a, int b) {  // clamped
 // One (group, head group, shared partition) unit: warp w of the CTA takes
 // head blockIdx.y * WARPS + w; smem is 1024-byte aligned, PrefixCfg::SMEM - 1024
 // bytes long.
+// A 16-token stage is a 16-row box of one block (block size 16 or 32), two
+// 8-row boxes of two blocks (block size 8: each box fills one 1 KB swizzle
+// atom), or, with 4-token blocks (half an atom), 16-byte cp.async copies by
+// the lanes into the same swizzled rows.  part_tokens is a multiple of 16
+// (the caller runs other partitions as private ones).
 template <int D, int BS, int WARPS>
 __device__ __forceinline__ void prefix_partition(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                                  const DecodeArgs& a, int grp, int part,
                                                  uint8_t* smem) {
   using Cfg = PrefixCfg<D, WARPS>;
-  constexpr int SUB = BS / kTB;
-  static_assert(BS % kTB == 0, "block size must be a multiple of 16");
+  constexpr int SUB = BS >= kTB ? BS / kTB : 1;  // stages per block
+  constexpr int BPS = BS >= kTB ? 1 : kTB / BS;  // blocks per stage
+  constexpr bool kGatherCp = BS < 8;
+  static_assert(BS % kTB == 0 || kTB % BS == 0, "block size divides 16 or 16 divides it");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * WARPS + warp;
   if (h >= a.H) return;
@@ -165,19 +186,55 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap& kmap, const 
   }
   __syncwarp();
   auto issue = [&](int u, int s) {
-    const int pb = __shfl_sync(kPfxFull, phys, u / SUB);
-    if (lane == 0) {
-      uint8_t* st = wbase + s * Cfg::STAGE;
-      const int row = pb * BS + (u % SUB) * kTB;
-      mbar_arrive_expect_tx(&bars[s], Cfg::STAGE);
+    uint8_t* st = wbase + s * Cfg::STAGE;
+    if constexpr (kGatherCp) {
+      // Row r of the stage is token u * 16 + r of the partition; every lane
+      // takes (row, 16-byte chunk) pairs of K and of V; one cp.async group
+      // per stage.  Rows of an out-of-range block read as zeros.
+      constexpr int kChunks = D / 8;
 #pragma unroll
-      for (int sl = 0; sl < Cfg::SLABS; ++sl) {
-        tma_load_3d(st + sl * Cfg::SLAB_BYTES, &kmap, sl * 64, h, row, &bars[s]);
-        tma_load_3d(st + Cfg::TILE + sl * Cfg::SLAB_BYTES, &vmap, sl * 64, h, row, &bars[s]);
+      for (int i = lane; i < kTB * kChunks; i += 32) {
+        const int r = i / kChunks, c = i % kChunks;
+        const int pb = __shfl_sync(kPfxFull, phys, (u * kTB + r) / BS);
+        const size_t src = (((size_t)pb * BS + r % BS) * a.H + h) * D + c * 8;
+        uint8_t* dk = st + sw_off(r, c);
+        if (pb < a.num_blocks) {
+          cp_async16(dk, a.k_cache + src);
+          cp_async16(dk + Cfg::TILE, a.v_cache + src);
+        } else {
+          *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(dk + Cfg::TILE) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      cp_async_commit();
+    } else {
+      int pb[BPS];
+#pragma unroll
+      for (int k = 0; k < BPS; ++k) pb[k] = __shfl_sync(kPfxFull, phys, (u * BPS + k) / SUB);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[s], Cfg::STAGE);
+#pragma unroll
+        for (int k = 0; k < BPS; ++k) {
+          const int row = pb[k] * BS + (u % SUB) * kTB;  // first row of the box
+          const int r0 = k * (kTB / BPS);                 // its row in the stage
+#pragma unroll
+          for (int sl = 0; sl < Cfg::SLABS; ++sl) {
+            tma_load_3d(st + sl * Cfg::SLAB_BYTES + r0 * 128, &kmap, sl * 64, h, row, &bars[s]);
+            tma_load_3d(st + Cfg::TILE + sl * Cfg::SLAB_BYTES + r0 * 128, &vmap, sl * 64, h,
+                        row, &bars[s]);
+          }
+        }
       }
     }
   };
-  for (int u = 0; u < kStages && u < nunit; ++u) issue(u, u);
+  // (cp.async gathers: one group per stage, an empty one past the end, so
+  // that waiting for all but the last kStages - 1 groups completes stage u.)
+  for (int u = 0; u < kStages; ++u) {
+    if (u < nunit)
+      issue(u, u);
+    else if constexpr (kGatherCp)
+      cp_async_commit();
+  }
 
   float o[Cfg::NT_O][4];
 #pragma unroll
@@ -190,7 +247,12 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap& kmap, const 
   int u = 0;
   for (; u < nunit; ++u) {
     const int s = u % kStages;
-    if (!__all_sync(kPfxFull, mbar_wait(&bars[s], (u / kStages) & 1))) break;
+    if constexpr (kGatherCp) {
+      cp_async_wait_pfx<kStages - 1>();  // this lane's copies of stage u landed
+      __syncwarp();                       // ... and every other lane's
+    } else {
+      if (!__all_sync(kPfxFull, mbar_wait(&bars[s], (u / kStages) & 1))) break;
+    }
     const uint32_t kb = smem_u32(wbase + s * Cfg::STAGE);
     const uint32_t vb = kb + Cfg::TILE;
 
@@ -249,10 +311,13 @@ __device__ __forceinline__ void prefix_partition(const CUtensorMap& kmap, const 
     __syncwarp();
     const int nxt = u + kStages;
     if (nxt < nunit) {
-      if (lane == 0) fence_proxy_async_smem();
+      if (!kGatherCp && lane == 0) fence_proxy_async_smem();
       issue(nxt, s);
+    } else if constexpr (kGatherCp) {
+      cp_async_commit();
     }
   }
+  if constexpr (kGatherCp) cp_async_wait_pfx<0>();
   if (u < nunit) {
     if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
     for (int j = u; j < nunit && j < u + kStages; ++j)

@@ -66,7 +66,8 @@ def run_shared(q, kc, vc, bt, ctx, groups, gmax, pt, scale, status=None):
                                       partition_tokens=pt)
 
 
-@pytest.mark.parametrize("D,bs", [(128, 16), (128, 32), (64, 16)])
+@pytest.mark.parametrize("D,bs", [(128, 16), (128, 32), (64, 16), (128, 8), (64, 8), (128, 4),
+                                  (64, 4)])
 def test_shared_prefix_matches_oracle(D, bs):
     sizes = [1, 3, 16, 2]
     prefix_blocks = [4, 8, 6, 1]
@@ -78,7 +79,9 @@ def test_shared_prefix_matches_oracle(D, bs):
     scale = 1.0 / np.sqrt(D)
     ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), bt, ctx, scale)
     status = zero_status(DEV)
-    for pt in (2 * bs, 4 * bs, 32 * bs):  # shared partitions vary, one-partition case included
+    # shared partitions vary, one-partition case included; below 16 tokens per
+    # block also partitions that are no multiple of 16 (not shared, per member)
+    for pt in sorted({2 * bs, 4 * bs, 8 * bs, 32 * bs}):
         out = run_shared(q, kc, vc, bt, ctx, groups, gmax, pt, scale, status)
         assert_close(out, ref, what=f"shared prefix D={D} bs={bs} pt={pt}")
     torch.cuda.synchronize()
