@@ -57,13 +57,13 @@ L2_FLUSH_BYTES = 512 << 20
 # any of them changes.
 TRAFFIC = {
     # partition_kernel<128,16,4,2,fp16> with the fused write, 38-sequence step
-    ("llama13b_decode", 16, "6529d41896991a6d"): 853227008 + 5955584,
+    ("llama13b_decode", 16, "d37909182f59135c"): 853272064 + 5894400,
     # the grouped partition kernel of the 16 x 8 prefix-sharing batch
-    ("prefix_sharing", 16, "6529d41896991a6d"): 1093453056 + 10859264,
+    ("prefix_sharing", 16, "d37909182f59135c"): 1093385216 + 10804736,
     # partition kernel over a 65,536-token context, scaled by tokens (x16)
-    ("long_context", 16, "6529d41896991a6d"): (1342286848 + 6921472) * 16,
+    ("long_context", 16, "d37909182f59135c"): (1342303744 + 7040256) * 16,
     # the e4m3 partition kernel, 38-sequence batch
-    ("llama13b_decode_fp8", 16, "6529d41896991a6d"): 440090112 + 5027328,
+    ("llama13b_decode_fp8", 16, "d37909182f59135c"): 440134400 + 5250048,
     # prefill_kernel<128,16>, 8 x 512 queries on 3,584 cached tokens
     ("chunked_prefill", 16, "c1384d1ebac96fb1"): 713183232 + 35681536,
 }
