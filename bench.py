@@ -179,7 +179,8 @@ class Nvml:
 
 class ClockSampler:
     """Polls the SM clock and the clock-event reasons every ~5 ms (NVML) from
-    a thread; windows() marks the timed regions whose samples are reported."""
+    a thread; summary() reports the samples that fall inside given windows
+    (the timed regions, as perf_counter intervals)."""
 
     def __init__(self, device):
         self.samples = []  # (perf_counter time, sm MHz, max MHz, reasons mask)
@@ -431,7 +432,7 @@ def workload_config(batch):
             "sum_context_len": int(ctx.sum())}
 
 
-def run_gpu(args, rank, world, local_rank, sampler):
+def run_gpu(args, rank, world, local_rank):
     import paged_kv_cache_172_gb300 as pk
     from paged_kv_cache_172_gb300.session import DecodeSession
 
@@ -1014,7 +1015,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     sampler = ClockSampler(dev).start()
     try:
-        res = run_gpu(args, rank, world, local_rank, sampler)
+        res = run_gpu(args, rank, world, local_rank)
         K = args.steps
         total_s = res["step_ms"] * K / 1e3
         step_bytes = res["step_bytes"]
