@@ -57,15 +57,15 @@ L2_FLUSH_BYTES = 512 << 20
 # any of them changes.
 TRAFFIC = {
     # partition_kernel<128,16,4,2,fp16> with the fused write, 38-sequence step
-    ("llama13b_decode", 16, "d37909182f59135c"): 853272064 + 5894400,
+    ("llama13b_decode", 16, "f8b2784f8d52dcd5"): 853226752 + 5956608,
     # the grouped partition kernel of the 16 x 8 prefix-sharing batch
-    ("prefix_sharing", 16, "d37909182f59135c"): 1093385216 + 10804736,
+    ("prefix_sharing", 16, "f8b2784f8d52dcd5"): 1093573120 + 10993408,
     # partition kernel over a 65,536-token context, scaled by tokens (x16)
-    ("long_context", 16, "d37909182f59135c"): (1342303744 + 7040256) * 16,
-    # the e4m3 partition kernel, 38-sequence batch
-    ("llama13b_decode_fp8", 16, "d37909182f59135c"): 440134400 + 5250048,
+    ("long_context", 16, "f8b2784f8d52dcd5"): (1342286336 + 6832128) * 16,
+    # the e4m3 partition kernel (two heads per warp), 38-sequence batch
+    ("llama13b_decode_fp8", 16, "f8b2784f8d52dcd5"): 440002816 + 4989952,
     # prefill_kernel<128,16>, 8 x 512 queries on 3,584 cached tokens
-    ("chunked_prefill", 16, "c1384d1ebac96fb1"): 713183232 + 35681536,
+    ("chunked_prefill", 16, "eb9cebd1c9e42ff0"): 713334528 + 36440832,
 }
 TRAFFIC_SOURCES = {
     "llama13b_decode": ("decode.cu", "pk_common.cuh", "pk_prefix.cuh", "pk_internal.h"),

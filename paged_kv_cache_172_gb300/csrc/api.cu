@@ -266,7 +266,10 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
   const long long rows = (long long)num_blocks * block_size;
   pk::DecodeMaps maps;
   memset(&maps, 0, sizeof(maps));
-  const int box_tokens = pk::decode_box_tokens(fp8 != nullptr, block_size);
+  // e4m3 boxes span the heads of a warp (two adjacent ones for an even head
+  // count), fp16 boxes one head.
+  const int hpw = pk::decode_heads_per_warp(fp8 != nullptr, H);
+  const int box_tokens = pk::decode_box_tokens(fp8 != nullptr, block_size, hpw);
   cudaError_t e;
   if (fp8 == nullptr) {
     e = pk::make_pool_map(&maps.k, k_cache, rows, H, D, 1, box_tokens);
@@ -276,7 +279,7 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
                                         (unsigned long long)rows};
     const unsigned long long strides[2] = {(unsigned long long)D,
                                            (unsigned long long)H * D};
-    const unsigned box[3] = {(unsigned)D, 1, (unsigned)box_tokens};
+    const unsigned box[3] = {(unsigned)D, (unsigned)hpw, (unsigned)box_tokens};
     e = pk::make_map_3d(&maps.k, fp8->k8, dims, strides, box, false,
                         CU_TENSOR_MAP_DATA_TYPE_UINT8);
     if (e == cudaSuccess)
@@ -286,7 +289,7 @@ static pa_status decode_impl(const pa_half* q, const pa_half* k_new, const pa_ha
                                          (unsigned long long)num_blocks};
     const unsigned long long sstrides[2] = {(unsigned long long)block_size * 4,
                                             (unsigned long long)H * block_size * 4};
-    const unsigned sbox[3] = {(unsigned)box_tokens, 1, 1};
+    const unsigned sbox[3] = {(unsigned)box_tokens, (unsigned)hpw, 1};
     if (e == cudaSuccess)
       e = pk::make_map_3d(&maps.ks, fp8->k_scale, sdims, sstrides, sbox, false,
                           CU_TENSOR_MAP_DATA_TYPE_FLOAT32);

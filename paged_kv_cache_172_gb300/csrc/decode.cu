@@ -109,14 +109,12 @@ __device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t w, uint32_t& lo, uint
   hi = *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Lane partial of q . k for EPL e4m3 codes of k (fp16 query pairs qh); from 16
-// dims on, two interleaved sums shorten the dependent chain.
+// Lane partial of q . k for EPL e4m3 codes of k (EPL / 4 words w; fp16 query
+// pairs qh); from 16 dims on, two interleaved sums shorten the dependent chain.
 template <int EPL>
-__device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) {
+__device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint32_t* w) {
   static_assert(EPL % 4 == 0, "whole words of codes");
   constexpr int NW = EPL / 4, NACC = EPL >= 16 ? 2 : 1;
-  uint32_t w[NW];
-  load_words<NW>(w, p);
   float t[NACC];
 #pragma unroll
   for (int k = 0; k < NACC; ++k) t[k] = 0.f;
@@ -131,15 +129,13 @@ __device__ __forceinline__ float dot_e4m3(const uint32_t* qh, const uint8_t* p) 
   return t[0];
 }
 
-// o[e] += w * v[e] for EPL e4m3 codes v (exact in fp16), products exact in
-// fp32, one rounding per addition.
+// o[e] += w * v[e] for EPL e4m3 codes v (EPL / 4 words wd; exact in fp16),
+// products exact in fp32, one rounding per addition.
 template <int EPL>
-__device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint8_t* p) {
+__device__ __forceinline__ void axpy_e4m3(float* o, __half w, const uint32_t* wd) {
   static_assert(EPL % 4 == 0, "whole words of codes");
   constexpr int NW = EPL / 4;
   const uint16_t wb = __half_as_ushort(w);
-  uint32_t wd[NW];
-  load_words<NW>(wd, p);
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
     uint32_t lo, hi;
@@ -194,84 +190,126 @@ __device__ __forceinline__ int checked_ctx(const DecodeArgs& a, int b, bool repo
 #define PK_DECODE_FP8_RL 8
 #endif
 #ifndef PK_DECODE_FP8_TB
-#define PK_DECODE_FP8_TB 32  // e4m3 tokens per stage at block size >= 16
+#define PK_DECODE_FP8_TB 32  // e4m3 rows per stage at block size >= 16
+#endif
+#ifndef PK_DECODE_FP8_HPW
+#define PK_DECODE_FP8_HPW 2  // heads per e4m3 warp when the head count is even
 #endif
 
-// Tokens per TMA box of a stage (the maps' box): 16 fp16 rows; e4m3 rows up
-// to the stage size (the whole block at the default 32-token stages); below
-// block size 16, one block.
-constexpr int box_tokens_for(bool fp8, int bs) {
-  return (fp8 ? (bs >= 16 ? PK_DECODE_FP8_TB : bs) : (bs < 16 ? bs : 16)) < bs
-             ? (fp8 ? (bs >= 16 ? PK_DECODE_FP8_TB : bs) : (bs < 16 ? bs : 16))
-             : bs;
+// Tokens per pipeline stage: 16 fp16 rows, or PK_DECODE_FP8_TB / hpw e4m3
+// tokens (hpw heads each) at block size >= 16; below 16, one block.
+constexpr int stage_tokens_for(bool fp8, int bs, int hpw) {
+  return fp8 ? (bs >= 16 ? PK_DECODE_FP8_TB / hpw : bs) : (bs < 16 ? bs : 16);
+}
+// Tokens per TMA box of a stage (the maps' box): a stage's tokens, at most
+// one block.
+constexpr int box_tokens_for(bool fp8, int bs, int hpw) {
+  return stage_tokens_for(fp8, bs, hpw) < bs ? stage_tokens_for(fp8, bs, hpw) : bs;
 }
 
-template <int D, int BS, int WARPS, int NSTAGE, bool FP8>
+// Copy each stage to registers before its arithmetic and refill it at once
+// (bit 0: fp16 pools, bit 1: e4m3 pools).
+#ifndef PK_DECODE_STAGE_REGS
+#define PK_DECODE_STAGE_REGS 0
+#endif
+
+// HPW: heads per warp.  An e4m3 row of one (token, head) is D bytes (128 at
+// D = 128), and HBM serves such 128-byte pieces about 7 % slower than 256-byte
+// ones, so with an even head count each e4m3 warp takes two adjacent heads:
+// its boxes read both heads' rows of a token, 2 D contiguous bytes.  The two
+// warps of a pair then split the partition's stages (even and odd ones) and
+// merge their results at the end, so a warp still streams one head's worth
+// of a partition and the grid keeps its number of work units.
+template <int D, int BS, int WARPS, int NSTAGE, bool FP8, int HPW = 1>
 struct PartitionCfg {
-  // Tokens per pipeline stage: 16 fp16 rows (4 KB per head at D = 128), or 32
-  // e4m3 rows at block size >= 16 -- the same bytes per stage, and every lane
-  // then holds a distinct token's score, so the per-stage reductions cost half
-  // as much per token.  A TMA box never spans blocks: TBX tokens, BPS per stage.
-  static constexpr int TB = FP8 ? (BS >= 16 ? PK_DECODE_FP8_TB : BS) : (BS < 16 ? BS : 16);
-  // Lanes covering one token's D dims: 32 for fp16; 8 for e4m3 (four tokens
-  // per warp instruction, 16 codes per lane: one 16-byte shared-memory read per
-  // token and lane, eight lanes per 128-byte row, so no bank conflicts; three
-  // butterfly rounds per stage instead of four at 16 lanes), at least 32 / TB so
-  // that a stage still fills one warp instruction.
-  static constexpr int RL = !FP8 ? 32 : (PK_DECODE_FP8_RL * TB >= 32 ? PK_DECODE_FP8_RL : 32 / TB);
-  static constexpr int NT = 32 / RL;                  // tokens per warp instruction
+  static_assert(HPW == 1 || (FP8 && HPW == 2), "two heads per warp for e4m3 pools only");
+  // Tokens per pipeline stage: 16 fp16 tokens (4 KB per head at D = 128), or
+  // 32 / HPW e4m3 tokens at block size >= 16 -- the same bytes per stage, and
+  // every lane then holds a distinct row's score, so the per-stage reductions
+  // cost half as much per row.  A row is one (token, head), HPW rows per token.
+  // A TMA box never spans blocks: TBX tokens, BPS per stage.
+  static constexpr int TB = stage_tokens_for(FP8, BS, HPW);
+  static constexpr int ROWS = TB * HPW;               // rows per stage
+  // Lanes covering one row's D dims: 32 for fp16; 8 for e4m3 (four rows per
+  // warp instruction, 16 codes per lane: one 16-byte shared-memory read per
+  // row and lane, eight lanes per 128-byte row, so no bank conflicts; three
+  // butterfly rounds per stage instead of four at 16 lanes), at least 32 / ROWS
+  // so that a stage still fills one warp instruction.
+  static constexpr int RL =
+      !FP8 ? 32 : (PK_DECODE_FP8_RL * ROWS >= 32 ? PK_DECODE_FP8_RL : 32 / ROWS);
+  static constexpr int NT = 32 / RL;                  // rows per warp instruction
+  // Row it * NT + lane / RL of a stage is head (lane / RL) % HPW of its token:
+  // a lane stays on one head.
+  static_assert(NT % HPW == 0, "each lane keeps one head");
   static constexpr int EPL = D / RL;                  // dims per lane
   static constexpr int TBX = TB < BS ? TB : BS;       // tokens per TMA box
-  static_assert(TBX == box_tokens_for(FP8, BS), "the maps' box is one stage box");
+  static_assert(TBX == box_tokens_for(FP8, BS, HPW), "the maps' box is one stage box");
   static constexpr int BPS = TB / TBX;                // boxes per tensor per stage
   static constexpr int SUB = BS / TBX;                // boxes per physical block
   static constexpr int ELEM = FP8 ? 1 : 2;            // bytes per stored K/V element
-  static constexpr int TILE_BYTES = TB * D * ELEM;    // one head's rows of one stage
-  static constexpr int SCALE_BYTES = FP8 ? TB * 4 : 0;  // per-token scales of one stage
-  // Scales of one tensor and stage: box k of TBX tokens at byte k * 128 (a TMA
-  // destination in shared memory must be 128-byte aligned).
+  static constexpr int TILE_BYTES = ROWS * D * ELEM;  // the rows of one stage
+  static constexpr int SCALE_BYTES = FP8 ? ROWS * 4 : 0;  // per-row scales of one stage
+  // Scales of one tensor and stage: box k ([HPW heads][TBX tokens]) at byte
+  // k * 128 (a TMA destination in shared memory must be 128-byte aligned).
   static constexpr int SCALE_SLOT = FP8 ? BPS * 128 : 0;
-  static_assert(!FP8 || TBX * 4 <= 128, "one box of scales per 128-byte slot");
-  // Float index of token t's scale inside a scale slot.
-  static __device__ __forceinline__ int scale_index(int t) { return (t / TBX) * 32 + t % TBX; }
+  static_assert(!FP8 || TBX * HPW * 4 <= 128, "one box of scales per 128-byte slot");
+  // Float index of row r's scale inside a scale slot.
+  static __device__ __forceinline__ int scale_index(int r) {
+    const int t = r / HPW;
+    return (t / TBX) * 32 + (r % HPW) * TBX + t % TBX;
+  }
   // stage = [K rows][V rows][K scales][V scales]; TX_BYTES actually land
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SCALE_SLOT;
   static constexpr int TX_BYTES = 2 * TILE_BYTES + 2 * SCALE_BYTES;
   static_assert(TILE_BYTES % 128 == 0 && STAGE_BYTES % 128 == 0, "TMA destinations 128-B aligned");
-  static constexpr int LANES_PER_TOKEN = 32 / TB;     // lanes sharing a score after the butterfly
+  static constexpr int LANES_PER_ROW = 32 / ROWS > 1 ? 32 / ROWS : 1;  // lanes sharing a score
   static constexpr int SMEM_BYTES = WARPS * NSTAGE * STAGE_BYTES + WARPS * NSTAGE * 8;
 };
 
 // GRP: grouped call (a.seq_group set) that also runs shared-prefix partitions;
 // a separate instantiation so plain decode keeps its small register budget.
-template <int D, int BS, int WARPS, int NSTAGE, bool FP8, bool GRP = false>
+// HPW: heads per warp (two: e4m3 pools with an even head count).
+template <int D, int BS, int WARPS, int NSTAGE, bool FP8, bool GRP = false, int HPW = 1>
 __global__ void __launch_bounds__(WARPS * 32)
     partition_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
-  using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE, FP8>;
+  using Cfg = PartitionCfg<D, BS, WARPS, NSTAGE, FP8, HPW>;
   constexpr int EPL = Cfg::EPL;
   constexpr int TB = Cfg::TB;
   constexpr int SUB = Cfg::SUB;
-  constexpr int LPT = Cfg::LANES_PER_TOKEN;
+  constexpr int LPR = Cfg::LANES_PER_ROW;
   constexpr int RL = Cfg::RL, NT = Cfg::NT;
-  constexpr int ITER = TB / NT;  // warp instructions per stage (one token per RL lanes each)
-  static_assert(ITER >= 1 && RL % ITER == 0, "stage tokens vs row lanes");
+  constexpr int ITER = Cfg::ROWS / NT;  // warp instructions per stage (one row per RL lanes each)
+  static_assert(ITER >= 1 && RL % ITER == 0, "stage rows vs row lanes");
+  constexpr int KWORDS = EPL * Cfg::ELEM / 4;  // 32-bit words of a lane's slice of one row
+  constexpr bool kStageRegs = ((FP8 ? 2 : 1) & PK_DECODE_STAGE_REGS) != 0;
   static_assert(BS >= 1 && BS <= 32 && (32 % BS) == 0, "block_size must divide 32");
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x;
-  const int h = blockIdx.y * WARPS + warp;
+  static_assert(WARPS % HPW == 0, "whole warp pairs");
+  const int th = warp % HPW;                         // the pair's stages this warp takes
+  const int h0 = blockIdx.y * WARPS + warp - th;     // the warp's first head (WARPS per CTA)
+  const int h = h0 + (lane / RL) % HPW;              // the head of this lane's rows
   const int part = blockIdx.z;
-  pdl_wait();            // inputs may come from the previous kernel on the stream
-  if (h >= a.H) return;  // idle warp of a ragged head group (no CTA-wide sync below)
+  pdl_wait();             // inputs may come from the previous kernel on the stream
+  if (h0 >= a.H) return;  // idle warp of a ragged head group (no CTA-wide sync below)
 
   uint8_t* wbase = smem + warp * NSTAGE * Cfg::STAGE_BYTES;
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + WARPS * NSTAGE * Cfg::STAGE_BYTES) + warp * NSTAGE;
 
-  const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
   const int tok0 = part * a.part_tokens;
+  const int lb0 = tok0 / BS;
+  // The partition's block-table entries (one per lane, at most 32) are read
+  // together with the context length, before it is known, so that the first
+  // copies wait for one round trip to memory instead of two; entries past the
+  // context are never looked at.
+  int tab = 0;
+  if (lane < min(a.part_tokens / BS, a.max_blocks - lb0))
+    tab = a.block_tables[(size_t)b * a.max_blocks + lb0 + lane];
+  const int ctx = checked_ctx(a, b, lane == 0 && part == 0);
   const size_t row_bh = (size_t)b * a.H + h;
   // Partitions inside a group's shared prefix (partitions of whole 16-token
   // stages; with other partition sizes every member computes its own).
@@ -293,28 +331,29 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
   if (tok0 >= ctx) {
-    if (part == 0 && lane < RL) {  // empty sequence: zero row
+    if (part == 0 && th == 0 && lane < RL * HPW) {  // empty sequence: zero rows
       float z[EPL] = {};
-      store_half_row<EPL>(a.out + row_bh * D + lane * EPL, z);
+      store_half_row<EPL>(a.out + row_bh * D + (lane % RL) * EPL, z);
     }
     return;
   }
   const int tok1 = min(ctx, tok0 + a.part_tokens);
-  const int lb0 = tok0 / BS;
   const int nblk = (tok1 - tok0 + BS - 1) / BS;  // <= 32 by construction of part_tokens
   const int nunit = (tok1 - tok0 + TB - 1) / TB; // pipeline stages (TB-token sub-blocks)
+  // Stages of this warp: units th, th + HPW, ... of the partition.
+  const int nmine = (nunit - th + HPW - 1) / HPW;
 
   // Block-table entries of this partition, one per lane.
   int phys = 0;
   if (lane < nblk) {
-    phys = a.block_tables[(size_t)b * a.max_blocks + lb0 + lane];
+    phys = tab;
     if (phys < 0 || phys >= a.num_blocks) {
       flag_status(a.status, PA_DEV_BAD_BLOCK_ID);
       phys = a.num_blocks;  // entirely outside the tensor map: TMA fills zeros
     }
   }
 
-  // Dims [dl, dl + EPL) of this lane; lane / RL picks the token of a pair.
+  // Dims [dl, dl + EPL) of this lane; lane / RL picks the row of an instruction.
   const int dl = (lane % RL) * EPL;
 
   if (lane == 0) {
@@ -325,7 +364,8 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   // Prologue: fill the pipeline.  Unit u is tokens [u*TB, u*TB+TB) of the
   // partition; its box k holds tokens u*TB + k*TBX + [0, TBX), inside logical
-  // block lb0 + (u*TB + k*TBX) / BS.
+  // block lb0 + (u*TB + k*TBX) / BS, for the warp's HPW heads ([token][head]
+  // rows; scales [head][token]).
   auto issue = [&](int u, int s) {  // all lanes (shuffle), lane 0 issues
     uint8_t* st = wbase + s * Cfg::STAGE_BYTES;
     if (lane == 0) mbar_arrive_expect_tx(&bars[s], Cfg::TX_BYTES);
@@ -335,18 +375,18 @@ __global__ void __launch_bounds__(WARPS * 32)
       const int pb = __shfl_sync(kFull, phys, tt / BS);
       if (lane == 0) {
         const int row = pb * BS + tt % BS;
-        tma_load_3d(st + k * Cfg::TBX * D * Cfg::ELEM, &maps.k, 0, h, row, &bars[s]);
-        tma_load_3d(st + Cfg::TILE_BYTES + k * Cfg::TBX * D * Cfg::ELEM, &maps.v, 0, h, row,
-                    &bars[s]);
-        if constexpr (FP8) {  // scales [num_blocks, H, bs]: box of TBX tokens
-          tma_load_3d(st + 2 * Cfg::TILE_BYTES + k * 128, &maps.ks, tt % BS, h, pb, &bars[s]);
-          tma_load_3d(st + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT + k * 128, &maps.vs, tt % BS, h,
-                      pb, &bars[s]);
+        constexpr int kBoxBytes = Cfg::TBX * HPW * D * Cfg::ELEM;
+        tma_load_3d(st + k * kBoxBytes, &maps.k, 0, h0, row, &bars[s]);
+        tma_load_3d(st + Cfg::TILE_BYTES + k * kBoxBytes, &maps.v, 0, h0, row, &bars[s]);
+        if constexpr (FP8) {  // scales [num_blocks, H, bs]: box of HPW x TBX
+          tma_load_3d(st + 2 * Cfg::TILE_BYTES + k * 128, &maps.ks, tt % BS, h0, pb, &bars[s]);
+          tma_load_3d(st + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT + k * 128, &maps.vs, tt % BS,
+                      h0, pb, &bars[s]);
         }
       }
     }
   };
-  for (int i = 0; i < NSTAGE && i < nunit; ++i) issue(i, i);
+  for (int i = 0; i < NSTAGE && i < nmine; ++i) issue(i * HPW + th, i);
 
   // Query slice of this lane (and, for e4m3 pools, its fp16 pairs), read once
   // the first stages are in flight so that its latency overlaps the K/V copies.
@@ -365,10 +405,12 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
   for (int e = 0; e < EPL; ++e) o[e] = 0.f;
 
-  // Token whose score this lane holds after the butterfly (lane / LPT for RL = 32).
+  // Row whose score this lane holds after the butterfly (lane / LPR for RL =
+  // 32); it is a row of the lane's own head.
   const int my_tok = ((lane % RL) / (RL / ITER)) * NT + lane / RL;
   int i = 0;
-  for (; i < nunit; ++i) {
+  for (; i < nmine; ++i) {
+    const int u = i * HPW + th;  // unit of the partition
     const int s = i % NSTAGE;
     const uint32_t parity = (i / NSTAGE) & 1;
     const bool got = mbar_wait(&bars[s], parity);
@@ -379,14 +421,15 @@ __global__ void __launch_bounds__(WARPS * 32)
     __half* vs = reinterpret_cast<__half*>(kst + Cfg::TILE_BYTES);
     const float* kscl = reinterpret_cast<const float*>(kst + 2 * Cfg::TILE_BYTES);
     const float* vscl = reinterpret_cast<const float*>(kst + 2 * Cfg::TILE_BYTES + Cfg::SCALE_SLOT);
-    const int valid = min(TB, tok1 - (tok0 + i * TB));  // tokens of this unit inside the partition
+    const int valid = min(TB, tok1 - (tok0 + u * TB));  // tokens of this unit inside the partition
+    const int valid_rows = valid * HPW;  // rows are [token][head]
 
     // Appending: the new token (position ctx-1) is scored from k_new/v_new,
     // copied over the stage row TMA brought in, and stored to its cache slot.
     if constexpr (!FP8) {
-      const int t_new = ctx - 1 - (tok0 + i * TB);
+      const int t_new = ctx - 1 - (tok0 + u * TB);
       if (a.k_new != nullptr && t_new >= 0 && t_new < TB) {
-        const int pb = __shfl_sync(kFull, phys, i / SUB);
+        const int pb = __shfl_sync(kFull, phys, u / SUB);
         const size_t src = row_bh * D + lane * EPL;
         LaneVec<EPL> kn, vn;
         kn.load(a.k_new + src);
@@ -394,7 +437,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         *reinterpret_cast<decltype(kn.raw)*>(ks + t_new * D + lane * EPL) = kn.raw;
         *reinterpret_cast<decltype(vn.raw)*>(vs + t_new * D + lane * EPL) = vn.raw;
         if (pb < a.num_blocks) {
-          const size_t slot = (size_t)pb * BS + (i % SUB) * TB + t_new;
+          const size_t slot = (size_t)pb * BS + (u % SUB) * TB + t_new;
           const size_t dst = (slot * a.H + h) * D + lane * EPL;
           *reinterpret_cast<decltype(kn.raw)*>(a.k_cache + dst) = kn.raw;
           *reinterpret_cast<decltype(vn.raw)*>(a.v_cache + dst) = vn.raw;
@@ -403,21 +446,55 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
     }
 
+    // This lane's K and V data of the stage: its dims of the tokens of every
+    // warp instruction (EPL fp16 values or EPL e4m3 codes each) and, for e4m3
+    // pools, the scales of the token whose score it will hold.  With kStageRegs
+    // they are copied to registers first and the stage is refilled at once,
+    // so the copy of unit i + NSTAGE overlaps this unit's arithmetic instead
+    // of waiting for it.
+    uint32_t kw[ITER][KWORDS], vw[ITER][KWORDS];
+    auto load_k = [&](int it) {
+      const int t = it * NT + lane / RL;
+      load_words<KWORDS>(kw[it], kst + (t * D + dl) * Cfg::ELEM);
+    };
+    auto load_v = [&](int it) {
+      const int t = it * NT + lane / RL;
+      load_words<KWORDS>(vw[it], kst + Cfg::TILE_BYTES + (t * D + dl) * Cfg::ELEM);
+    };
+    [[maybe_unused]] float ksc = 1.f, vsc = 1.f;
+    if constexpr (kStageRegs) {
+#pragma unroll
+      for (int it = 0; it < ITER; ++it) {
+        load_k(it);
+        load_v(it);
+      }
+      if constexpr (FP8) {
+        ksc = kscl[Cfg::scale_index(my_tok)];
+        vsc = vscl[Cfg::scale_index(my_tok)];
+      }
+      __syncwarp();
+      const int nxt = i + NSTAGE;
+      if (nxt < nmine) {
+        if (lane == 0) fence_proxy_async_smem();
+        issue(nxt * HPW + th, s);
+      }
+    }
+
     // Partial dot products: instruction it covers token it * NT + lane / RL.
     float part_dot[ITER];
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
-      const int t = it * NT + lane / RL;
+      if constexpr (!kStageRegs) load_k(it);
       if constexpr (FP8) {
-        part_dot[it] = dot_e4m3<EPL>(qh, kst + t * D + dl);
+        part_dot[it] = dot_e4m3<EPL>(qh, kw[it]);
       } else {
-        float kf[EPL];
-        LaneVec<EPL> kv;
-        kv.load(ks + t * D + dl);
-        kv.to_float(kf);
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+        for (int e = 0; e < EPL / 2; ++e) {
+          const float2 kf = __half22float2(*reinterpret_cast<const __half2*>(&kw[it][e]));
+          acc = fmaf(qf[2 * e], kf.x, acc);
+          acc = fmaf(qf[2 * e + 1], kf.y, acc);
+        }
         part_dot[it] = acc;
       }
     }
@@ -439,13 +516,25 @@ __global__ void __launch_bounds__(WARPS * 32)
       part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
 
     float dot = part_dot[0];
-    if constexpr (FP8) dot *= kscl[Cfg::scale_index(my_tok)];  // per-(token, head) scale
-    float sc = (my_tok < valid) ? dot * a.scale_log2 : -INFINITY;
-    const float m_new = fmaxf(m, warp_max(sc));
+    if constexpr (FP8) {  // per-(token, head) scale
+      if constexpr (!kStageRegs) ksc = kscl[Cfg::scale_index(my_tok)];
+      dot *= ksc;
+    }
+    float sc = (my_tok < valid_rows) ? dot * a.scale_log2 : -INFINITY;
+    float mx;  // this stage's maximum of the lane's head
+    if constexpr (HPW == 1) {
+      mx = warp_max(sc);
+    } else {
+      const bool second = ((lane / RL) & 1) != 0;
+      const float m0 = warp_max(second ? -INFINITY : sc);
+      const float m1 = warp_max(second ? sc : -INFINITY);
+      mx = second ? m1 : m0;
+    }
+    const float m_new = fmaxf(m, mx);
     const float alpha = fast_exp2(m - m_new);
-    const float pr = (my_tok < valid) ? fast_exp2(sc - m_new) : 0.f;
-    // Each lane keeps the sum of its own tokens' weights (alpha is uniform
-    // over the warp); the lanes are summed once, after the last stage.
+    const float pr = (my_tok < valid_rows) ? fast_exp2(sc - m_new) : 0.f;
+    // Each lane keeps the sum of its own rows' weights (alpha is uniform over
+    // the lanes of a head); the lanes are summed once, after the last stage.
     l = l * alpha + pr;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
@@ -454,45 +543,74 @@ __global__ void __launch_bounds__(WARPS * 32)
     // until the partition writes it.  The lane holding a token's score forms
     // its weight; instruction it broadcasts the weights of its NT tokens.
     float wv = pr;
-    if constexpr (FP8) wv = __uint_as_float((uint32_t)__half_as_ushort(
-                           __float2half_rn(pr * 256.f * vscl[Cfg::scale_index(my_tok)])));
+    if constexpr (FP8) {
+      if constexpr (!kStageRegs) vsc = vscl[Cfg::scale_index(my_tok)];
+      wv = __uint_as_float((uint32_t)__half_as_ushort(__float2half_rn(pr * 256.f * vsc)));
+    }
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
       const int t = it * NT + lane / RL;
       const float pt = __shfl_sync(kFull, wv, (lane / RL) * RL + it * (RL / ITER));
-      if (t < valid) {
+      if (t < valid_rows) {
+        if constexpr (!kStageRegs) load_v(it);
         if constexpr (FP8) {
-          axpy_e4m3<EPL>(o, __ushort_as_half((unsigned short)__float_as_uint(pt)),
-                         kst + Cfg::TILE_BYTES + t * D + dl);
+          axpy_e4m3<EPL>(o, __ushort_as_half((unsigned short)__float_as_uint(pt)), vw[it]);
         } else {
-          float vf[EPL];
-          LaneVec<EPL> vv;
-          vv.load(vs + t * D + dl);
-          vv.to_float(vf);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, vf[e], o[e]);
+          for (int e = 0; e < EPL / 2; ++e) {
+            const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&vw[it][e]));
+            o[2 * e] = fmaf(pt, vf.x, o[2 * e]);
+            o[2 * e + 1] = fmaf(pt, vf.y, o[2 * e + 1]);
+          }
         }
       }
     }
     m = m_new;
 
-    // Refill this stage with unit i + NSTAGE.
-    __syncwarp();
-    const int nxt = i + NSTAGE;
-    if (nxt < nunit) {
-      if (lane == 0) fence_proxy_async_smem();
-      issue(nxt, s);
+    if constexpr (!kStageRegs) {  // refill this stage with unit i + NSTAGE
+      __syncwarp();
+      const int nxt = i + NSTAGE;
+      if (nxt < nmine) {
+        if (lane == 0) fence_proxy_async_smem();
+        issue(nxt * HPW + th, s);
+      }
     }
   }
 
   pdl_launch_dependents();  // the combine kernel may be scheduled now
-  if (i < nunit) {
+  bool ok = i >= nmine;
+  if (!ok) {
     // A bounded wait gave up: report, drain what is still in flight (again
     // bounded) so no copy lands after the CTA exits, and write nothing.
     if (lane == 0) flag_status(a.status, PA_DEV_TIMEOUT);
-    for (int j = i; j < nunit && j < i + NSTAGE; ++j) mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
-    return;
+    for (int j = i; j < nmine && j < i + NSTAGE; ++j) mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
   }
+  if constexpr (HPW == 2) {
+    // Merge the pair's two halves lane by lane (the same head and dims): the
+    // odd-stage warp leaves (m, l, o) in its own, now idle, stage room.  Both
+    // warps always reach the barrier, so a wait that gave up in one of them
+    // cannot leave the other waiting.
+    float* xch = reinterpret_cast<float*>(smem + (warp - th + 1) * NSTAGE * Cfg::STAGE_BYTES) +
+                 lane * (EPL + 2);
+    if (th == 1 && ok) {
+      xch[0] = m;
+      xch[1] = l;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) xch[2 + e] = o[e];
+    }
+    ok = named_bar_and(1 + warp / 2, 64, ok);
+    if (th == 1) return;
+    if (ok) {
+      const float m1 = xch[0];
+      const float mm = fmaxf(m, m1);  // finite: the even warp has at least one stage
+      const float w0 = fast_exp2(m - mm), w1 = fast_exp2(m1 - mm);
+      l = l * w0 + xch[1] * w1;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[e] = o[e] * w0 + xch[2 + e] * w1;
+      m = mm;
+    }
+  }
+  if (!ok) return;
 
   if constexpr (FP8) {
 #pragma unroll
@@ -501,9 +619,10 @@ __global__ void __launch_bounds__(WARPS * 32)
   // Lanes whose tokens differ: their weight sums, and (e4m3: several tokens
   // per instruction) their o rows for the same dims.
 #pragma unroll
-  for (int off = LPT; off <= 16; off <<= 1) l += __shfl_xor_sync(kFull, l, off);
+  for (int off = LPR; off <= 16; off <<= 1)
+    if (HPW == 1 || off != RL) l += __shfl_xor_sync(kFull, l, off);  // lanes of one head
 #pragma unroll
-  for (int off = RL; off < 32; off <<= 1)
+  for (int off = RL * HPW; off < 32; off <<= 1)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] += __shfl_xor_sync(kFull, o[e], off);
   const int n_parts = (ctx + a.part_tokens - 1) / a.part_tokens;
@@ -512,11 +631,11 @@ __global__ void __launch_bounds__(WARPS * 32)
     float r[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) r[e] = o[e] * inv;
-    if (lane < RL) store_half_row<EPL>(a.out + row_bh * D + dl, r);
+    if (lane < RL * HPW) store_half_row<EPL>(a.out + row_bh * D + dl, r);
   } else {
     const size_t row = row_bh * a.num_parts + part;
     float* dst = a.ws_o + row * D + dl;
-    if (lane < RL) {
+    if (lane < RL * HPW) {
       if constexpr (EPL % 4 == 0) {
 #pragma unroll
         for (int i = 0; i < EPL / 4; ++i)
@@ -525,7 +644,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
       }
     }
-    if (lane == 0) *reinterpret_cast<float2*>(a.ws_ml + row * 2) = make_float2(m, l);
+    if (lane % RL == 0 && lane < RL * HPW)
+      *reinterpret_cast<float2*>(a.ws_ml + row * 2) = make_float2(m, l);
   }
 }
 
@@ -684,7 +804,7 @@ __global__ void __launch_bounds__(kMaxCombineWarps * 32) combine_kernel(const De
 #define PK_DECODE_FP8_NSTAGE 2
 #endif
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, int HPW = 1>
 struct DecodeTuning {
   static constexpr int WARPS = PK_DECODE_WARPS;
   static constexpr int STAGE = 2 * (BS < 16 ? BS : 16) * D * 2;
@@ -694,10 +814,11 @@ struct DecodeTuning {
   static constexpr int RAW = PK_DECODE_INFLIGHT_BYTES / STAGE;
   static constexpr int NSTAGE16 = RAW < 2 ? 2 : (RAW > 8 ? 8 : RAW);
 #endif
-  // e4m3 stages of 32 tokens hold as many bytes as 16 fp16 tokens: two per
+  // e4m3 stages of 32 rows hold as many bytes as 16 fp16 tokens: two per
   // warp, as for fp16, keeps three CTAs per SM (three stages leave two).
-  // Below block size 16 a stage is one block: enough of them for the bytes.
-  static constexpr int STAGE8 = 2 * BS * D;
+  // Below block size 16 a stage is one block (HPW heads): enough of them for
+  // the bytes.
+  static constexpr int STAGE8 = 2 * BS * HPW * D;
   static constexpr int RAW8 = PK_DECODE_INFLIGHT_BYTES / STAGE8;
   static constexpr int NSTAGE = !FP8 ? NSTAGE16
                                      : (BS >= 16 ? PK_DECODE_FP8_NSTAGE
@@ -724,6 +845,19 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The partition grid of an ungrouped call with HPW heads per warp.
+template <int D, int BS, bool FP8, int HPW>
+cudaError_t launch_partitions(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream) {
+  using T = DecodeTuning<D, BS, FP8, HPW>;
+  using Cfg = PartitionCfg<D, BS, T::WARPS, T::NSTAGE, FP8, HPW>;
+  constexpr auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8, false, HPW>;
+  cudaError_t e = ensure_dynamic_smem<kern>(Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  // WARPS heads per CTA either way (with HPW = 2, two pairs of two warps)
+  return launch_pdl(kern, dim3(a.B, (a.H + T::WARPS - 1) / T::WARPS, a.num_parts),
+                    dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
+}
+
 template <int D, int BS, bool FP8>
 cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream) {
   using T = DecodeTuning<D, BS, FP8>;
@@ -733,10 +867,12 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeMaps& maps, cudaStr
   bool grouped = false;
   if constexpr (!FP8) grouped = a.seq_group != nullptr;
   if (!grouped) {
-    constexpr auto kern = partition_kernel<D, BS, T::WARPS, T::NSTAGE, FP8>;
-    e = ensure_dynamic_smem<kern>(Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, grid, dim3(T::WARPS * 32), Cfg::SMEM_BYTES, stream, maps, a);
+    if constexpr (FP8) {
+      e = decode_heads_per_warp(true, a.H) == 2 ? launch_partitions<D, BS, true, 2>(a, maps, stream)
+                                                : launch_partitions<D, BS, true, 1>(a, maps, stream);
+    } else {
+      e = launch_partitions<D, BS, false, 1>(a, maps, stream);
+    }
   } else if constexpr (!FP8) {
     // The grouped grid also runs the shared-prefix partitions.
     constexpr int kPfxSmem = pfx::PrefixCfg<D, T::WARPS>::SMEM;
@@ -766,7 +902,13 @@ bool prefix_supported(int D, int block_size, int max_group_size) {
          max_group_size >= 1 && max_group_size <= pfx::kMaxMembers;
 }
 
-int decode_box_tokens(bool fp8, int block_size) { return box_tokens_for(fp8, block_size); }
+int decode_heads_per_warp(bool fp8, int H) {
+  return fp8 && PK_DECODE_FP8_HPW == 2 && H % 2 == 0 ? 2 : 1;
+}
+
+int decode_box_tokens(bool fp8, int block_size, int heads_per_warp) {
+  return box_tokens_for(fp8, block_size, heads_per_warp);
+}
 
 bool decode_supported(int D, int block_size) {
   return (D == 64 || D == 128) &&

@@ -97,9 +97,12 @@ cudaError_t make_map_5d(CUtensorMap* map, const void* base, const unsigned long 
 // prefix partitions (multi-query, from maps.ksw / maps.vsw).
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps& maps, cudaStream_t stream);
 bool decode_supported(int D, int block_size);
+// Heads per warp of the decode partition kernel (2: e4m3 pools with an even
+// head count, whose K/V and scale boxes then span two adjacent heads).
+int decode_heads_per_warp(bool fp8, int H);
 // Tokens per TMA box of the decode partition kernel's stages (the box of the
 // K/V and scale maps must match it).
-int decode_box_tokens(bool fp8, int block_size);
+int decode_box_tokens(bool fp8, int block_size, int heads_per_warp);
 bool prefix_supported(int D, int block_size, int max_group_size);
 
 cudaError_t launch_kv_cache_write(const __half* k, const __half* v, const int64_t* slots, int T,

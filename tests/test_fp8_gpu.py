@@ -94,6 +94,21 @@ def test_fp8_decode_parity_and_accuracy(D, bs):
     assert rel.max() <= FP8_REL_L2_MAX and rel.mean() <= FP8_REL_L2_MEAN
 
 
+@pytest.mark.parametrize("H,bs", [(3, 16), (5, 32), (1, 4)])
+def test_fp8_decode_odd_head_count(H, bs):
+    # an odd head count: one head per warp (even counts pair adjacent heads)
+    ctx = [1, 15, 16, 17, 300, 777]
+    batch = workloads.random_decode(len(ctx), H, 128, bs, ctx, seed=95 + H, device="cpu")
+    k8, v8, ks, vs = quantize_pool(batch)
+    ref8 = oracle.decode_fp8(batch.q.numpy(), k8.cpu().numpy(), v8.cpu().numpy(),
+                             ks.cpu().numpy(), vs.cpu().numpy(), batch.block_tables.numpy(),
+                             batch.context_lens.numpy(), batch.scale)
+    for pt in (0, 2 * bs):
+        out = pk.pa_decode_fp8(batch.q.to(DEV), k8, v8, ks, vs, batch.block_tables.to(DEV),
+                               batch.context_lens.to(DEV), batch.scale, 777, partition_tokens=pt)
+        assert_close(out, ref8, what=f"fp8 decode H={H} bs={bs} pt={pt}")
+
+
 def test_fp8_llama13b_batch():
     batch = workloads.llama13b_decode(seed=1, device=DEV)
     k8, v8, ks, vs = quantize_pool(batch)
