@@ -9,11 +9,13 @@ right summation); this module only marshals numpy arrays into it.  fp16
 inputs are passed as their raw 16-bit patterns and decoded exactly in C.
 
 Functions and the passages they follow (page titles and sections):
-  attend_row / decode / prefill -- blog "PagedAttention origin and evolution"
+  attend_row / decode / prefill / prefill_varlen -- blog "PagedAttention origin and evolution"
       sec. 3.2.2 (forward pass: gather through the block table, scale by
       1/sqrt(head_dim), softmax, weighted V) and tutorial chapter
       "4. PagedAttention机制：vLLM的核心创新", section "PagedAttention的注意力计算";
-      prefill uses the end-aligned causal reading of the sec. 3.2.2 mask.
+      prefill uses the end-aligned causal reading of the sec. 3.2.2 mask;
+      prefill_varlen is that prefill per sequence on its own chunk length
+      (the sec. 3.2.2 forward pass takes each request's queries separately).
   kv_cache_write -- the same tutorial, section "Block管理策略" (the cache grows
       into newly mapped blocks); slot = physical_block * block_size + offset.
   block_copy -- study notes "DataWhale组队学习笔记--llm-algo-leetcode(五)",
@@ -32,7 +34,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = [
-    "OracleError", "half_to_double", "attend_row", "decode", "prefill",
+    "OracleError", "half_to_double", "attend_row", "decode", "prefill", "prefill_varlen",
     "kv_cache_write", "block_copy", "gather", "load", "e4m3_to_double", "e4m3_from_float",
     "kv_cache_write_fp8", "decode_fp8",
 ]
@@ -165,6 +167,28 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, scale, lib=None):
     _check(lib.oracle_prefill(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl),
                               B, H, Lq, D, bs, nb, bt.shape[1], float(scale),
                               _ptr(out)))
+    return out
+
+
+def prefill_varlen(q, k_cache, v_cache, block_tables, context_lens, q_lens, scale, lib=None):
+    """Chunks of different lengths: q[B,H,Lq,D] fp16 holds sequence b's
+    q_lens[b] new queries in rows 0 .. q_lens[b]-1 (the last q_lens[b]
+    positions of its context, end-aligned causal mask).  Each sequence is
+    the fixed-length prefill of its own rows; rows past q_lens[b] are zero.
+    -> out[B,H,Lq,D] fp64."""
+    qb = _bits(q)
+    B, H, Lq, D = qb.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32).reshape(B, -1)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32).reshape(B)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int64).reshape(B)
+    if np.any(ql < 0) or np.any(ql > Lq) or np.any(ql > cl):
+        raise OracleError(3)
+    out = np.zeros((B, H, Lq, D), dtype=np.float64)
+    for b in range(B):
+        n = int(ql[b])
+        if n > 0:
+            out[b:b + 1, :, :n] = prefill(qb[b:b + 1, :, :n], k_cache, v_cache, bt[b:b + 1],
+                                          cl[b:b + 1], scale, lib)
     return out
 
 

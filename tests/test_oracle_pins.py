@@ -268,6 +268,28 @@ def check_prefill_lq1_is_decode(lib):
     assert np.array_equal(a, b)
 
 
+def check_prefill_varlen_rows_are_decodes(lib):
+    """Query i of a chunk of n new queries on a context of c keys is a decode
+    over keys 0 .. c-n+i; padded rows are zero; equal lengths give prefill."""
+    rng = np.random.default_rng(27)
+    B, H, D, bs, Lq = 4, 2, 16, 4, 6
+    k, v, tables, ctx = paged_case(rng, B, H, D, bs, [9, 6, 13, 3])
+    q = rand16(rng, (B, H, Lq, D))
+    q_lens = [4, 6, 0, 3]
+    out = oracle.prefill_varlen(q, k, v, tables, ctx, q_lens, 0.3, lib=lib)
+    for b in range(B):
+        n, c = q_lens[b], int(ctx[b])
+        assert np.all(out[b, :, n:] == 0.0)
+        for i in range(n):
+            row = oracle.decode(q[b:b + 1, :, i], k, v, tables[b:b + 1], [c - n + i + 1], 0.3,
+                                lib=lib)[0]
+            assert np.array_equal(out[b, :, i], row)
+    full = oracle.prefill_varlen(q[:, :, :3], k, v, tables, ctx, [3, 3, 3, 3], 0.3, lib=lib)
+    assert np.array_equal(full, oracle.prefill(q[:, :, :3], k, v, tables, ctx, 0.3, lib=lib))
+    with pytest.raises(oracle.OracleError):  # more new queries than keys
+        oracle.prefill_varlen(q, k, v, tables, ctx, [4, 6, 0, 4], 0.3, lib=lib)
+
+
 def check_permutation_invariance(lib):
     rng = np.random.default_rng(18)
     k, v, tables, ctx = paged_case(rng, 3, 2, 16, 4, [7, 12, 3], spare=5)
@@ -427,7 +449,8 @@ ALL_CHECKS = [
     check_closed_form_uniform, check_single_key_and_ones,
     check_two_keys_logistic, check_scale_zero_mean, check_dense_decode,
     check_dense_prefill, check_prefill_whole_context_is_tril,
-    check_prefill_lq1_is_decode, check_permutation_invariance,
+    check_prefill_lq1_is_decode, check_prefill_varlen_rows_are_decodes,
+    check_permutation_invariance,
     check_cache_write, check_block_copy, check_e4m3_decode, check_e4m3_encode,
     check_fp8_quantize, check_fp8_decode_dense,
 ]
