@@ -357,6 +357,30 @@ pa_status pa_prefill_chunk(const pa_half *q, const pa_half *k_cache,
                            int32_t *status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Chunked prefill with a chunk length per sequence.
+ *
+ * The same computation as pa_prefill_chunk for sequence b's q_lens[b] new
+ * queries, which sit in rows 0 .. q_lens[b]-1 of its [H, Lq_max, D] slice
+ * of q: query i is at position n - q_lens[b] + i (n = context_lens[b]) and
+ * attends to keys 0 .. n - q_lens[b] + i (the blog's sec. 3.2.2 forward pass
+ * takes each request's queries on their own).  Rows q_lens[b] .. Lq_max-1
+ * of out are written as zeros.  q_lens is [B] int32 on the device (or in
+ * mapped page-locked host memory), each in [0, Lq_max] and at most
+ * context_lens[b]; a sequence breaking that is flagged PA_DEV_BAD_CONTEXT in
+ * *status and its rows are zeros.  q_lens NULL (with B, Lq_max > 0) returns
+ * PA_ERR_INVALID.  Every other argument, the workspace rule (with
+ * pa_prefill_workspace_size(B, H, Lq_max, D)) and the error behaviour are
+ * those of pa_prefill_chunk with Lq = Lq_max.
+ * ------------------------------------------------------------------------- */
+pa_status pa_prefill_chunk_varlen(const pa_half *q, const pa_half *k_cache,
+                                  const pa_half *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, const int32_t *q_lens,
+                                  int B, int H, int Lq_max, int D, int block_size,
+                                  int num_blocks, int max_blocks_per_seq, float scale,
+                                  pa_half *out, void *workspace, size_t workspace_bytes,
+                                  int32_t *status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Cache write (scatter new tokens' K/V into their slots).
  *
  * With the caches viewed as [num_blocks * block_size, H, D], for each token

@@ -23,7 +23,8 @@ PA_DEV_TIMEOUT = 0x10
 EXPORTS = (
     "pa_status_string", "pa_last_cuda_error", "pa_version", "pa_host_device_pointer",
     "pa_decode_partition_tokens", "pa_decode_workspace_size", "pa_decode",
-    "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_kv_cache_write", "pa_block_copy",
+    "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_prefill_chunk_varlen",
+    "pa_kv_cache_write", "pa_block_copy",
     "pa_decode_static",
     "pa_decode_append", "pa_decode_shared_prefix", "pa_shared_prefix_groups",
     "pa_kv_cache_write_fp8", "pa_decode_fp8",
@@ -66,6 +67,9 @@ def _bind(lib):
     lib.pa_prefill_chunk.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      ctypes.c_float, _P, _P, _SZ, _P, _P]
     lib.pa_prefill_chunk.restype = _I
+    lib.pa_prefill_chunk_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                            ctypes.c_float, _P, _P, _SZ, _P, _P]
+    lib.pa_prefill_chunk_varlen.restype = _I
     lib.pa_kv_cache_write.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.pa_kv_cache_write.restype = _I
     lib.pa_block_copy.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
@@ -369,12 +373,18 @@ def pa_prefill_workspace_size(B, H, Lq, D):
 
 
 def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-                     workspace=None, tail_split=True, status=None, stream=None):
+                     workspace=None, tail_split=True, status=None, stream=None, q_lens=None):
     """Chunked prefill attention.  q [B,H,Lq,D] fp16 are the last Lq positions
     of each sequence (end-aligned causal mask).  Returns out [B,H,Lq,D].
-    A workspace for the tail split is allocated when not given; tail_split=False
-    passes none (every work unit runs whole)."""
+    With q_lens ([B] int32 on the device), sequence b has q_lens[b] <= Lq new
+    queries in rows 0 .. q_lens[b]-1 and its later rows of out are zeros
+    (pa_prefill_chunk_varlen).  A workspace for the tail split is allocated
+    when not given; tail_split=False passes none (every work unit runs whole)."""
     _need(q, torch.float16, "q", 4)
+    if q_lens is not None:
+        _need(q_lens, torch.int32, "q_lens", 1)
+        if q_lens.numel() != q.shape[0]:
+            raise ValueError("q_lens must have one entry per sequence")
     _need(k_cache, torch.float16, "k_cache", 4)
     _need(v_cache, torch.float16, "v_cache", 4)
     _need(block_tables, torch.int32, "block_tables", 2)
@@ -394,11 +404,20 @@ def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out
         if ws_bytes > 0:
             workspace = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device=q.device)
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                _ptr(context_lens), B, H, Lq, D, bs, NB,
-                                block_tables.shape[1], float(scale), _ptr(out), _ptr(workspace),
-                                ws_len, _ptr(status), _stream(stream, q.device))
-    _check(rc, "pa_prefill_chunk")
+    if q_lens is None:
+        rc = lib().pa_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                    _ptr(context_lens), B, H, Lq, D, bs, NB,
+                                    block_tables.shape[1], float(scale), _ptr(out),
+                                    _ptr(workspace), ws_len, _ptr(status),
+                                    _stream(stream, q.device))
+        _check(rc, "pa_prefill_chunk")
+    else:
+        rc = lib().pa_prefill_chunk_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_tables), _ptr(context_lens), _ptr(q_lens),
+                                           B, H, Lq, D, bs, NB, block_tables.shape[1],
+                                           float(scale), _ptr(out), _ptr(workspace), ws_len,
+                                           _ptr(status), _stream(stream, q.device))
+        _check(rc, "pa_prefill_chunk_varlen")
     return out
 
 

@@ -449,11 +449,14 @@ size_t pa_prefill_workspace_size(int B, int H, int Lq, int D) {
   return pk::prefill_workspace_bytes(B, H, Lq, D);
 }
 
-pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
-                           const int32_t* block_tables, const int32_t* context_lens, int B, int H,
-                           int Lq, int D, int block_size, int num_blocks, int max_blocks_per_seq,
-                           float scale, pa_half* out, void* workspace, size_t workspace_bytes,
-                           int32_t* status, pa_stream_t stream) {
+// Shared body of pa_prefill_chunk (q_lens null: Lq queries per sequence) and
+// pa_prefill_chunk_varlen.
+static pa_status prefill_impl(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              const int32_t* q_lens, int B, int H, int Lq, int D, int block_size,
+                              int num_blocks, int max_blocks_per_seq, float scale, pa_half* out,
+                              void* workspace, size_t workspace_bytes, int32_t* status,
+                              pa_stream_t stream) {
   if (B < 0 || H <= 0 || Lq < 0 || max_blocks_per_seq <= 0 || !isfinite(scale) ||
       !(scale > 0.f))
     return PA_ERR_INVALID;
@@ -475,6 +478,7 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
   a.ws_floats = workspace != nullptr ? workspace_bytes / sizeof(float) : 0;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
+  a.q_lens = q_lens;
   a.out = reinterpret_cast<__half*>(out);
   a.status = status;
   a.B = B;
@@ -488,6 +492,29 @@ pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_ha
   cudaError_t e = pk::launch_prefill(a, k_cache, v_cache, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return PA_ERR_INVALID;
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_prefill_chunk(const pa_half* q, const pa_half* k_cache, const pa_half* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, int B, int H,
+                           int Lq, int D, int block_size, int num_blocks, int max_blocks_per_seq,
+                           float scale, pa_half* out, void* workspace, size_t workspace_bytes,
+                           int32_t* status, pa_stream_t stream) {
+  return prefill_impl(q, k_cache, v_cache, block_tables, context_lens, nullptr, B, H, Lq, D,
+                      block_size, num_blocks, max_blocks_per_seq, scale, out, workspace,
+                      workspace_bytes, status, stream);
+}
+
+pa_status pa_prefill_chunk_varlen(const pa_half* q, const pa_half* k_cache,
+                                  const pa_half* v_cache, const int32_t* block_tables,
+                                  const int32_t* context_lens, const int32_t* q_lens, int B,
+                                  int H, int Lq_max, int D, int block_size, int num_blocks,
+                                  int max_blocks_per_seq, float scale, pa_half* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* status,
+                                  pa_stream_t stream) {
+  if (q_lens == nullptr && B > 0 && Lq_max > 0) return PA_ERR_INVALID;
+  return prefill_impl(q, k_cache, v_cache, block_tables, context_lens, q_lens, B, H, Lq_max, D,
+                      block_size, num_blocks, max_blocks_per_seq, scale, out, workspace,
+                      workspace_bytes, status, stream);
 }
 
 // ---------------------------------------------------------------------------

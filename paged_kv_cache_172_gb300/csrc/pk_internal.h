@@ -132,6 +132,9 @@ struct PrefillArgs {
   const __half* v_cache;  // the cp.async gather of blocks under 8 tokens)
   const int32_t* block_tables;
   const int32_t* context_lens;
+  // [B] new queries per sequence (<= Lq; rows past it are written as zeros),
+  // or null: Lq for every sequence
+  const int32_t* q_lens;
   __half* out;
   int32_t* status;
   int B, H, Lq, D, block_size, num_blocks, max_blocks;

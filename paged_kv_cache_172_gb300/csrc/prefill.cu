@@ -205,11 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   pdl_wait();  // inputs may come from the previous kernel on the stream
   const int n = a.context_lens[b];
+  const int ql = a.q_lens != nullptr ? a.q_lens[b] : a.Lq;  // this sequence's new queries
   const int q0 = ct * 2 * kTileM;
   const int rows_all = min(2 * kTileM, a.Lq - q0);
   const size_t out_row0 = ((size_t)b * a.H + h) * a.Lq + q0;
-  if (n < a.Lq || n > a.max_blocks * BS) {
-    if (threadIdx.x == 0 && part <= 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
+  const bool bad = ql < 0 || ql > a.Lq || n < ql || n > a.max_blocks * BS;
+  if (bad || q0 >= ql) {
+    // A bad length (flagged), or rows past this sequence's chunk only: zero
+    // rows (a whole unit) or an empty partial (a part; the combine writes
+    // the zeros).
+    if (bad && threadIdx.x == 0 && part <= 0) flag_status(a.status, PA_DEV_BAD_CONTEXT);
     if (part < 0) {
       uint4* o4 = reinterpret_cast<uint4*>(a.out + out_row0 * D);
       for (int i = threadIdx.x; i < rows_all * (D / 8); i += kThreads)
@@ -224,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Per Q tile (A = 0, B = 1): rows, sequence position of row 0, key tiles.
   // ntile_a <= ntile_b whenever tile B has rows.
-  const int rows_a = min(kTileM, a.Lq - q0);
-  const int rows_b = max(0, min(kTileM, a.Lq - (q0 + kTileM)));
-  const int pos0_a = n - a.Lq + q0;
+  const int rows_a = min(kTileM, ql - q0);
+  const int rows_b = max(0, min(kTileM, ql - (q0 + kTileM)));
+  const int pos0_a = n - ql + q0;
   const int pos0_b = pos0_a + kTileM;
   // Key tiles of the unit, then this CTA's range [kt0, kt0 + n_kv) of them;
   // ntile_a / ntile_b count the range's tiles each Q tile reads.
@@ -635,25 +640,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       wrow[D] = ntile > 0 ? m : -INFINITY;
       wrow[D + 1] = ntile > 0 ? l : 0.f;
-    } else if (ok && ntile > 0) {
+    } else if (ok && q0 + x * kTileM < a.Lq) {
       // The output tile goes through Q_X's room (free: every S product of X
-      // is done, since its last P V product is), swizzled like the TMA tiles,
-      // and leaves by TMA stores: one 16 KB copy per 64-dim half instead of
-      // scattered 16-byte stores per thread.  Rows past the chunk fall outside
-      // the tensor map and are not written.
-      tc::fence_after_sync();
-      const float inv = 1.f / l;
+      // is done, since its last P V product is; Q_X landed before any
+      // softmax started), swizzled like the TMA tiles, and leaves by TMA
+      // stores: one 16 KB copy per 64-dim half instead of scattered 16-byte
+      // stores per thread.  Rows past the tensor's Lq fall outside the map and
+      // are not written; rows past this sequence's chunk (chunks of different
+      // lengths) are written as zeros.
+      const bool live = row < (x ? rows_b : rows_a);
+      if (ntile > 0) tc::fence_after_sync();
+      const float inv = ntile > 0 ? 1.f / l : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {  // dims 32c .. 32c+31
         uint32_t o[32];
-        tc::ld_32x32(t_o + c * 32, o);
-        tc::wait_ld();
+        if (ntile > 0) {
+          tc::ld_32x32(t_o + c * 32, o);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
         uint32_t hv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           __half2 t = __floats2half2_rn(__uint_as_float(o[2 * i]) * inv,
                                         __uint_as_float(o[2 * i + 1]) * inv);
-          hv[i] = *reinterpret_cast<uint32_t*>(&t);
+          hv[i] = live ? *reinterpret_cast<uint32_t*>(&t) : 0u;
         }
         uint8_t* slab = orow + (c >> 1) * kSlabBytes;
 #pragma unroll
@@ -716,6 +729,8 @@ __global__ void __launch_bounds__(256)
   const int ct = unit % a.gx, h = (unit / a.gx) % a.H, b = unit / (a.gx * a.H);
   const int qi = ct * 2 * kTileM + r;
   if (qi >= a.Lq) return;
+  // rows past this sequence's chunk (chunks of different lengths): zeros
+  const bool live = qi < (a.q_lens != nullptr ? a.q_lens[b] : a.Lq);
   const float* base = a.ws + (size_t)su * a.split * (2 * kTileM) * kStride + (size_t)r * kStride;
   const size_t part_stride = (size_t)(2 * kTileM) * kStride;
   // All parts' loads issued together (split <= PK_PREFILL_MAX_SPLIT <= 8).
@@ -758,7 +773,7 @@ __global__ void __launch_bounds__(256)
       for (int e = 0; e < EPL; ++e) o[e] += wgt * ov[s][e];
     }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = L > 0.f && live ? 1.f / L : 0.f;
   __half* dst = a.out + (((size_t)b * a.H + h) * a.Lq + qi) * D + lane * EPL;
   if constexpr (EPL == 4) {
     __half2 h0 = __floats2half2_rn(o[0] * inv, o[1] * inv);

@@ -137,6 +137,16 @@ def test_prefill_validation(lib):
         rc = lib.pa_prefill_chunk(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 128, 16, 8,
                                   4, bad_scale, 0x1000, NULL, 0, NULL, NULL)
         assert rc == pk.PA_ERR_INVALID
+    # chunks of different lengths: q_lens is required; otherwise as pa_prefill_chunk
+    rc = lib.pa_prefill_chunk_varlen(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, NULL, 2, 4, 8, 128,
+                                     16, 8, 4, 0.1, 0x1000, NULL, 0, NULL, NULL)
+    assert rc == pk.PA_ERR_INVALID
+    rc = lib.pa_prefill_chunk_varlen(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 2, 4, 8, 96,
+                                     16, 8, 4, 0.1, 0x1000, NULL, 0, NULL, NULL)
+    assert rc == pk.PA_ERR_UNSUPPORTED
+    rc = lib.pa_prefill_chunk_varlen(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, NULL, 0, 4, 8, 128,
+                                     16, 8, 4, 0.1, 0x1000, NULL, 0, NULL, NULL)
+    assert rc == pk.PA_OK  # nothing to do
 
 
 def test_binding_rejects_cpu_tensors():
