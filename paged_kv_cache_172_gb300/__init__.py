@@ -12,5 +12,5 @@ from ._lib import (  # noqa: F401
     pa_decode_append,
     pa_decode_partition_tokens, pa_decode_shared_prefix, pa_decode_workspace_size,
     pa_shared_prefix_groups, pa_kv_cache_write, pa_kv_cache_write_fp8, pa_decode_fp8,
-    pa_prefill_chunk, pa_prefill_workspace_size, status_string,
+    pa_prefill_chunk, pa_prefill_chunk_varlen, pa_prefill_workspace_size, status_string,
 )

@@ -421,6 +421,17 @@ def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out
     return out
 
 
+def pa_prefill_chunk_varlen(q, k_cache, v_cache, block_tables, context_lens, q_lens, scale,
+                            out=None, workspace=None, tail_split=True, status=None,
+                            stream=None):
+    """Chunked prefill with a chunk length per sequence: q [B,H,Lq_max,D]
+    holds sequence b's q_lens[b] new queries in rows 0 .. q_lens[b]-1;
+    out rows past q_lens[b] are zeros."""
+    return pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out=out,
+                            workspace=workspace, tail_split=tail_split, status=status,
+                            stream=stream, q_lens=q_lens)
+
+
 def pa_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, status=None, stream=None):
     """Scatter k/v [T,H,D] fp16 into the caches at slot_mapping [T] int64."""
     _need(k, torch.float16, "k", 3)
