@@ -57,15 +57,15 @@ L2_FLUSH_BYTES = 512 << 20
 # any of them changes.
 TRAFFIC = {
     # partition_kernel<128,16,4,2,fp16> with the fused write, 38-sequence step
-    ("llama13b_decode", 16, "f8b2784f8d52dcd5"): 853226752 + 5956608,
+    ("llama13b_decode", 16, "5667b8c48d12ca6f"): 853226240 + 5877760,
     # the grouped partition kernel of the 16 x 8 prefix-sharing batch
-    ("prefix_sharing", 16, "f8b2784f8d52dcd5"): 1093573120 + 10993408,
+    ("prefix_sharing", 16, "5667b8c48d12ca6f"): 1093560320 + 10887680,
     # partition kernel over a 65,536-token context, scaled by tokens (x16)
-    ("long_context", 16, "f8b2784f8d52dcd5"): (1342286336 + 6832128) * 16,
+    ("long_context", 16, "5667b8c48d12ca6f"): (1342286848 + 6948864) * 16,
     # the e4m3 partition kernel (two heads per warp), 38-sequence batch
-    ("llama13b_decode_fp8", 16, "f8b2784f8d52dcd5"): 440002816 + 4989952,
+    ("llama13b_decode_fp8", 16, "5667b8c48d12ca6f"): 439982336 + 5391104,
     # prefill_kernel<128,16>, 8 x 512 queries on 3,584 cached tokens
-    ("chunked_prefill", 16, "eb9cebd1c9e42ff0"): 713334528 + 36440832,
+    ("chunked_prefill", 16, "69937be6b146e0e5"): 713209088 + 38543616,
 }
 TRAFFIC_SOURCES = {
     "llama13b_decode": ("decode.cu", "pk_common.cuh", "pk_prefix.cuh", "pk_internal.h"),
