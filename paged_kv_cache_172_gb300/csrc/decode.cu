@@ -26,6 +26,10 @@
 //    instead of 5 per token.
 //  * Online softmax in the log2 domain (scale * log2(e) folded into one
 //    multiply), fp32 accumulation of P V with the lane's D/32 dims.
+//  * e4m3 pools (pa_decode_fp8) with an even head count: a warp takes two
+//    adjacent heads (boxes of 2 D contiguous bytes per token), eight lanes
+//    per (token, head) row, and the two warps of a pair split the
+//    partition's stages and merge their softmax states at the end.
 //  * Optional append (pa_decode_append): the warp whose partition holds
 //    position ctx-1 stores the new token's K/V (its head's slice) to the
 //    cache slot the block table gives and scores it from registers-to-smem,
@@ -446,9 +450,9 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
     }
 
-    // This lane's K and V data of the stage: its dims of the tokens of every
+    // This lane's K and V data of the stage: its dims of the rows of every
     // warp instruction (EPL fp16 values or EPL e4m3 codes each) and, for e4m3
-    // pools, the scales of the token whose score it will hold.  With kStageRegs
+    // pools, the scales of the row whose score it will hold.  With kStageRegs
     // they are copied to registers first and the stage is refilled at once,
     // so the copy of unit i + NSTAGE overlaps this unit's arithmetic instead
     // of waiting for it.
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
     }
 
-    // Partial dot products: instruction it covers token it * NT + lane / RL.
+    // Partial dot products: instruction it covers row it * NT + lane / RL.
     float part_dot[ITER];
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
@@ -498,8 +502,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         part_dot[it] = acc;
       }
     }
-    // Transposing butterfly over the RL lanes of a token: after round r,
-    // lanes keep half of the remaining instructions' tokens.
+    // Transposing butterfly over the RL lanes of a row: after round r,
+    // lanes keep half of the remaining instructions' rows.
 #pragma unroll
     for (int cnt = ITER, off = RL / 2; cnt > 1; cnt >>= 1, off >>= 1) {
       const bool upper = (lane & off) != 0;
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         part_dot[k] = keep + __shfl_xor_sync(kFull, send, off);
       }
     }
-    // Remaining lanes of the same token hold disjoint dim ranges: sum them.
+    // Remaining lanes of the same row hold disjoint dim ranges: sum them.
 #pragma unroll
     for (int off = RL / ITER / 2; off >= 1; off >>= 1)
       part_dot[0] += __shfl_xor_sync(kFull, part_dot[0], off);
@@ -540,8 +544,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int e = 0; e < EPL; ++e) o[e] *= alpha;
     // e4m3 pools: the weight p * v_scale goes to fp16 (relative error 2^-11)
     // times 2^8, which keeps it in the normal fp16 range; o carries the 2^8
-    // until the partition writes it.  The lane holding a token's score forms
-    // its weight; instruction it broadcasts the weights of its NT tokens.
+    // until the partition writes it.  The lane holding a row's score forms
+    // its weight; instruction it broadcasts the weights of its NT rows.
     float wv = pr;
     if constexpr (FP8) {
       if constexpr (!kStageRegs) vsc = vscl[Cfg::scale_index(my_tok)];
@@ -616,8 +620,8 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] *= 1.f / 256.f;  // exact
   }
-  // Lanes whose tokens differ: their weight sums, and (e4m3: several tokens
-  // per instruction) their o rows for the same dims.
+  // Lanes whose rows differ (of the lane's own head): their weight sums, and
+  // (e4m3: several rows per instruction) their o rows for the same dims.
 #pragma unroll
   for (int off = LPR; off <= 16; off <<= 1)
     if (HPW == 1 || off != RL) l += __shfl_xor_sync(kFull, l, off);  // lanes of one head
