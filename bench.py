@@ -57,15 +57,15 @@ L2_FLUSH_BYTES = 512 << 20
 # any of them changes.
 TRAFFIC = {
     # partition_kernel<128,16,4,2,fp16> with the fused write, 38-sequence step
-    ("llama13b_decode", 16, "5667b8c48d12ca6f"): 853226240 + 5877760,
+    ("llama13b_decode", 16, "6926943ee2a6ce18"): 853313280 + 5961984,
     # the grouped partition kernel of the 16 x 8 prefix-sharing batch
-    ("prefix_sharing", 16, "5667b8c48d12ca6f"): 1093560320 + 10887680,
+    ("prefix_sharing", 16, "6926943ee2a6ce18"): 1093610240 + 10890240,
     # partition kernel over a 65,536-token context, scaled by tokens (x16)
-    ("long_context", 16, "5667b8c48d12ca6f"): (1342286848 + 6948864) * 16,
+    ("long_context", 16, "6926943ee2a6ce18"): (1342285568 + 6882304) * 16,
     # the e4m3 partition kernel (two heads per warp), 38-sequence batch
-    ("llama13b_decode_fp8", 16, "5667b8c48d12ca6f"): 439982336 + 5391104,
+    ("llama13b_decode_fp8", 16, "6926943ee2a6ce18"): 439972608 + 4957440,
     # prefill_kernel<128,16>, 8 x 512 queries on 3,584 cached tokens
-    ("chunked_prefill", 16, "69937be6b146e0e5"): 713209088 + 38543616,
+    ("chunked_prefill", 16, "69937be6b146e0e5"): 713279232 + 38438656,
 }
 TRAFFIC_SOURCES = {
     "llama13b_decode": ("decode.cu", "pk_common.cuh", "pk_prefix.cuh", "pk_internal.h"),
