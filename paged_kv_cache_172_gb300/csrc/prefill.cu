@@ -526,31 +526,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kbase = (kt0 + j) * kTileN;
       const bool diag = kbase + kTileN - 1 > pos0;  // some key here is past some row
       // The whole S row in registers; S_X is then free for S_X(j+1).
+      // The loads also give each 32-key chunk's maximum.
       uint32_t r[4][32];
+      float cm[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::ld_32x32(t_s + c * 32, r[c]);
+      for (int c = 0; c < 4; ++c) tc::ld_32x32_max(t_s + c * 32, r[c], cm[c]);
       tc::wait_ld();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[x]);  // one arrival per warp
-      if (diag) {  // keys past this row's position: -inf
+      float mt = max3f(cm[0], cm[1], fmaxf(cm[2], cm[3]));
+      if (diag) {  // keys past this row's position: -inf, and the maximum of the rest
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (kbase + c * 32 + i > pos) r[c][i] = __float_as_uint(-INFINITY);
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            mx[(i >> 1) & 7] = max3f(mx[(i >> 1) & 7], __uint_as_float(r[c][i]),
+                                     __uint_as_float(r[c][i + 1]));
+        mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2)
-          mx[(i >> 1) & 7] = max3f(mx[(i >> 1) & 7], __uint_as_float(r[c][i]),
-                                   __uint_as_float(r[c][i + 1]));
-      const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
-                             fmaxf(mx[6], mx[7])) * sl2;
+      mt *= sl2;
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + 8.0f;
       float alpha = 1.f;
