@@ -38,3 +38,25 @@ def to_dev(batch, dev, names=("q", "k_cache", "v_cache", "block_tables", "contex
 
 def zero_status(dev):
     return torch.zeros(1, dtype=torch.int32, device=dev)
+
+
+def spiked_decode_batch(D, bs, seed):
+    """Scores with jumps far past any rescale margin, spread over partitions:
+    queries u + noise (u = ones), chosen keys a * u (about a * D above the
+    rest).  Sequence 0: the spike at the last key; 1: spikes of growing size in
+    three partitions; 2: the largest score at key 0; 3: no spike; 4: every
+    eighth key far below the rest."""
+    ctx = [1024, 1024, 1024, 700, 900]
+    from paged_kv_cache_172_gb300 import workloads
+    batch = workloads.random_decode(len(ctx), 2, D, bs, ctx, seed=seed, device="cpu")
+    g = torch.Generator().manual_seed(seed)
+    batch.q = (1.0 + 0.25 * torch.randn(batch.q.shape, generator=g)).half()
+    per_nat = 1.0 / (D * batch.scale)
+    marks = {0: [(ctx[0] - 1, 45)], 1: [(100, 15), (400, 35), (700, 60)], 2: [(0, 60)],
+             4: [(p, -40) for p in range(0, ctx[4], 8)]}
+    for b, ms in marks.items():
+        for pos, nats in ms:
+            blk = int(batch.block_tables[b, pos // bs])
+            batch.k_cache[blk, pos % bs] = torch.full((2, D), nats * per_nat).half()
+    return batch
+

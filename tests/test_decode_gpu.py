@@ -15,7 +15,7 @@ import oracle
 import paged_kv_cache_172_gb300 as pk
 from oracle.allocator import BlockAllocator, Sequence_
 from paged_kv_cache_172_gb300 import workloads
-from pk_testutil import assert_close, bits, errors, to_dev, zero_status
+from pk_testutil import assert_close, bits, errors, spiked_decode_batch, to_dev, zero_status
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -286,3 +286,20 @@ def test_llama13b_batch_block32():
                         batch.v_cache.cpu().numpy(), batch.block_tables.cpu().numpy()[sel],
                         batch.context_lens.cpu().numpy()[sel], batch.scale)
     assert_close(out[torch.from_numpy(sel).to(DEV)], ref, what="llama13b bs=32")
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 8)])
+def test_decode_score_spikes(D, bs):
+    # partitions whose maxima differ by up to 60 nats: the per-partition
+    # softmax and the log-sum-exp merge must keep every weight finite
+    batch = spiked_decode_batch(D, bs, seed=70 + D + bs)
+    ref = oracle.decode(batch.q.numpy(), batch.k_cache.numpy(), batch.v_cache.numpy(),
+                        batch.block_tables.numpy(), batch.context_lens.numpy(), batch.scale)
+    assert np.all(np.isfinite(ref))
+    g = to_dev(batch, DEV)
+    for pt in (0, bs, 8 * bs):
+        status = zero_status(DEV)
+        out = run_decode(g, batch.scale, 1024, pt=pt, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_close(out, ref, what=f"score spikes D={D} bs={bs} pt={pt}")

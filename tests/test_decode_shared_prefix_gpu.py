@@ -150,3 +150,33 @@ def test_groups_from_block_tables(seed, bs, gmax):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert_close(out, ref, what=f"derived groups seed={seed} bs={bs} gmax={gmax}")
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 8)])
+def test_shared_prefix_score_spikes(D, bs):
+    # scores that jump by 15-60 nats inside the shared prefix (the group's
+    # MMA partitions, one running maximum per member) and in the private
+    # tails, merged across partitions by log-sum-exp
+    sizes, prefix_blocks = [3, 4], [8, 6]
+    tails = np.array([5, 3 * bs, 1, 2 * bs + 3, bs, 7, 4 * bs])
+    q, kc, vc, bt, ctx, groups, gmax = grouped_batch(sizes, prefix_blocks, tails, 2, D, bs,
+                                                     seed=73 + D)
+    gen = torch.Generator().manual_seed(74 + D)
+    q = (1.0 + 0.25 * torch.randn(q.shape, generator=gen)).half()
+    scale = 1.0 / np.sqrt(D)
+    per_nat = 1.0 / (D * scale)
+    marks = [(0, 3, 20), (0, 5 * bs, 40), (0, 8 * bs + 2, 60),  # group 0: prefix, then tail
+             (3, 2, 60), (3, 4 * bs + 1, 15),                   # group 1: largest first
+             (6, 6 * bs + 4 * bs - 1, 45)]                      # a member's last key
+    for b, pos, nats in marks:
+        assert pos < ctx[b]
+        blk = int(bt[b, pos // bs])
+        kc[blk, pos % bs] = torch.full((2, D), nats * per_nat).half()
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), bt, ctx, scale)
+    assert np.all(np.isfinite(ref))
+    status = zero_status(DEV)
+    for pt in (2 * bs, 4 * bs):
+        out = run_shared(q, kc, vc, bt, ctx, groups, gmax, pt, scale, status)
+        assert_close(out, ref, what=f"shared prefix spikes D={D} bs={bs} pt={pt}")
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0

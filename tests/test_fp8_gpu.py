@@ -9,7 +9,7 @@ import torch
 import oracle
 import paged_kv_cache_172_gb300 as pk
 from paged_kv_cache_172_gb300 import workloads
-from pk_testutil import assert_close, zero_status
+from pk_testutil import assert_close, spiked_decode_batch, zero_status
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -120,3 +120,22 @@ def test_fp8_llama13b_batch():
                              batch.block_tables.cpu().numpy()[sel],
                              batch.context_lens.cpu().numpy()[sel], batch.scale)
     assert_close(out[torch.from_numpy(sel).to(DEV)], ref8, what="fp8 llama13b")
+
+
+def test_fp8_decode_score_spikes():
+    # e4m3 keys whose scores jump by up to 60 nats across partitions (the
+    # spike rows quantize with their own per-(token, head) scale)
+    batch = spiked_decode_batch(128, 16, seed=95)
+    k8, v8, ks, vs = quantize_pool(batch)
+    ref8 = oracle.decode_fp8(batch.q.numpy(), k8.cpu().numpy(), v8.cpu().numpy(),
+                             ks.cpu().numpy(), vs.cpu().numpy(), batch.block_tables.numpy(),
+                             batch.context_lens.numpy(), batch.scale)
+    assert np.all(np.isfinite(ref8))
+    g = {"q": batch.q.to(DEV), "bt": batch.block_tables.to(DEV), "cl": batch.context_lens.to(DEV)}
+    for pt in (0, 16, 128):
+        status = zero_status(DEV)
+        out = pk.pa_decode_fp8(g["q"], k8, v8, ks, vs, g["bt"], g["cl"], batch.scale, 1024,
+                               partition_tokens=pt, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_close(out, ref8, what=f"fp8 score spikes pt={pt}")

@@ -277,3 +277,48 @@ def test_tail_split_two_units_per_head():
     assert_close(out_split[:, hs], ref, what="tail-split heads, two units each")
     e = errors(out_split, out_whole.float().cpu().numpy().astype(np.float64))
     assert e[0] <= 2e-3, e
+
+
+def spiked_batch(D, bs, seed):
+    """Scores with jumps far past the softmax's rescale margin: every query is
+    u + noise (u = ones) and chosen keys are a * u, so a key's score is about
+    a * D above the rest.  Sequence 0: a spike at the last key, masked for all
+    queries but the last.  Sequence 1: spikes of growing size in tiles with no
+    masked key (the running maximum jumps three times).  Sequence 2: the
+    largest score at key 0.  Sequence 3: spikes inside the chunk, each seen
+    only by the queries at or after it."""
+    Lq, ctx = 256, [1024, 1024, 1024, 600]
+    batch = workloads.random_prefill(4, 2, D, bs, Lq, ctx, seed=seed, device="cpu",
+                                     write_chunk=False)
+    g = torch.Generator().manual_seed(seed)
+    batch.q = (1.0 + 0.25 * torch.randn(batch.q.shape, generator=g)).half()
+    per_nat = 1.0 / (D * batch.scale)  # key multiple that adds one nat to the score
+    spikes = {0: [(ctx[0] - 1, 45)],
+              1: [(100, 15), (400, 35), (700, 60)],
+              2: [(0, 60)],
+              3: [(ctx[3] - Lq + 10, 30), (ctx[3] - Lq + 130, 50), (ctx[3] - Lq + 250, 70)]}
+    for b, marks in spikes.items():
+        for pos, nats in marks:
+            blk = int(batch.block_tables[b, pos // bs])
+            batch.k_cache[blk, pos % bs] = torch.full((2, D), nats * per_nat).half()
+    return batch
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 16), (128, 4)])
+@pytest.mark.parametrize("tail_split", [True, False])
+def test_prefill_score_spikes(D, bs, tail_split):
+    # the row maximum is taken from the tensor-memory load on tiles with no
+    # masked key and from the unmasked keys on diagonal tiles; scores that
+    # jump by 15-70 nats check both, and the rescaling of the output
+    batch = spiked_batch(D, bs, seed=60 + D + bs)
+    ref = oracle.prefill(batch.q.numpy(), batch.k_cache.numpy(), batch.v_cache.numpy(),
+                         batch.block_tables.numpy(), batch.context_lens.numpy(), batch.scale)
+    assert np.all(np.isfinite(ref))
+    g = to_dev(batch, DEV)
+    status = zero_status(DEV)
+    out = pk.pa_prefill_chunk(g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], batch.scale, status=status,
+                              tail_split=tail_split)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out, ref, what=f"score spikes D={D} bs={bs} split={tail_split}")
