@@ -259,7 +259,8 @@ pa_status pa_decode_append(const pa_half *q, const pa_half *k_new,
  * k_cache8, v_cache8  [num_blocks, block_size, H, D] uint8 (e4m3 codes)
  * k_scale, v_scale    [num_blocks, H, block_size] float32
  * pa_kv_cache_write_fp8 takes the same tokens and slots as
- * pa_kv_cache_write (fp16 k, v [T, H, D]) and writes codes and scales.
+ * pa_kv_cache_write (fp16 k, v [T, H, D]) and writes codes and scales;
+ * H at most 65535 (as for decode), else PA_ERR_INVALID.
  * pa_decode_fp8 computes pa_decode's result on the dequantized cache
  * (fp32 accumulation, fp16 output), same arguments, workspace and errors.
  * ------------------------------------------------------------------------- */

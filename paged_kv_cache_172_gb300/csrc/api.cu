@@ -413,7 +413,7 @@ pa_status pa_kv_cache_write_fp8(const pa_half* k, const pa_half* v, const int64_
                                 int T, int H, int D, int block_size, int num_blocks,
                                 uint8_t* k_cache8, uint8_t* v_cache8, float* k_scale,
                                 float* v_scale, int32_t* status, pa_stream_t stream) {
-  if (T < 0 || H <= 0 || D <= 0) return PA_ERR_INVALID;
+  if (T < 0 || H <= 0 || H > 65535 || D <= 0) return PA_ERR_INVALID;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
   if (T == 0) return PA_OK;

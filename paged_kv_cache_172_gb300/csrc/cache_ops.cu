@@ -98,7 +98,9 @@ __global__ void __launch_bounds__(kCopyThreads)
 // Quantizing write into e4m3 pools: one warp per (token, head) row; lane l
 // owns D/32 consecutive dims.  scale = max|row| / 448 (1 for a zero row),
 // code = e4m3(x / scale) rounded to nearest even (both divisions correctly
-// rounded single precision).  grid = (T, 2): K (0) or V (1).
+// rounded single precision).  grid = (T, 2, ceil(H / 8)): token, K (0) or V
+// (1), group of eight heads; every warp has one row, so a token's rows are
+// read at once instead of one after another.
 template <int D>
 __global__ void __launch_bounds__(kCopyThreads)
     kv_cache_write_fp8_kernel(const __half* __restrict__ k, const __half* __restrict__ v,
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kCopyThreads)
   const long long slot = slots[t];
   if (slot < 0) return;
   if (slot >= n_slots) {
-    if (threadIdx.x == 0 && blockIdx.y == 0) flag_status(status, PA_DEV_BAD_SLOT);
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) flag_status(status, PA_DEV_BAD_SLOT);
     return;
   }
   const long long blk = slot / bs, off = slot % bs;
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(kCopyThreads)
   uint8_t* dst_pool = blockIdx.y == 0 ? k8 : v8;
   float* scl = blockIdx.y == 0 ? ks : vs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < H; h += kCopyThreads / 32) {
+  const int h = blockIdx.z * (kCopyThreads / 32) + warp;
+  if (h < H) {
     const __half* src = src_pool + ((long long)t * H + h) * D + lane * EPL;
     float x[EPL];
 #pragma unroll
@@ -157,7 +160,7 @@ cudaError_t launch_kv_cache_write_fp8(const __half* k, const __half* v, const in
                                       int T, int H, int D, int block_size, long long n_slots,
                                       uint8_t* k8, uint8_t* v8, float* k_scale, float* v_scale,
                                       int32_t* status, cudaStream_t stream) {
-  dim3 grid(T, 2);
+  dim3 grid(T, 2, (H + kCopyThreads / 32 - 1) / (kCopyThreads / 32));
   if (D == 128)
     kv_cache_write_fp8_kernel<128><<<grid, kCopyThreads, 0, stream>>>(
         k, v, slots, H, block_size, n_slots, k8, v8, k_scale, v_scale, status);

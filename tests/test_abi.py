@@ -123,6 +123,14 @@ def test_copy_validation(lib):
                              NULL) == pk.PA_ERR_INVALID
     assert lib.pa_block_copy(0x1000, 0x1000, 0x1000, 0, 4, 128, 16, 8, NULL,
                              NULL) == pk.PA_OK
+    p = 0x1000  # any 16-byte aligned address: these calls return before touching memory
+    w8 = lambda T=4, H=4, D=128, k=p: lib.pa_kv_cache_write_fp8(k, p, p, T, H, D, 16, 8, p, p, p,
+                                                                 p, NULL, NULL)
+    assert w8(H=65536) == pk.PA_ERR_INVALID  # one grid row per eight heads
+    assert w8(H=0) == pk.PA_ERR_INVALID
+    assert w8(D=96) == pk.PA_ERR_UNSUPPORTED
+    assert w8(T=0) == pk.PA_OK
+    assert w8(k=NULL) == pk.PA_ERR_INVALID
 
 
 def test_prefill_validation(lib):
