@@ -39,8 +39,8 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
                : "memory");
 }
 
-// Copy `nvec` 16-byte vectors from src to dst, this CTA's share being the
-// vectors [chunk0, chunk0 + chunk) of the row.
+// Copy the 16-byte vectors [begin, end) from src to dst; thread x takes
+// begin + x, begin + x + kCopyThreads, ... with kUnroll loads in flight.
 __device__ __forceinline__ void copy_vectors(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                              long long begin, long long end) {
   for (long long base = begin + threadIdx.x; base < end; base += (long long)kCopyThreads * kUnroll) {
