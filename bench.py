@@ -65,7 +65,7 @@ TRAFFIC = {
     # the e4m3 partition kernel (two heads per warp), 38-sequence batch
     ("llama13b_decode_fp8", 16, "6926943ee2a6ce18"): 439972608 + 4957440,
     # prefill_kernel<128,16>, 8 x 512 queries on 3,584 cached tokens
-    ("chunked_prefill", 16, "9386010d94b97a5e"): 713354496 + 36269824,
+    ("chunked_prefill", 16, "974571cd2e30d09f"): 713150976 + 36221184,
 }
 TRAFFIC_SOURCES = {
     "llama13b_decode": ("decode.cu", "pk_common.cuh", "pk_prefix.cuh", "pk_internal.h"),

@@ -33,8 +33,9 @@
 // bounded that layout.
 // Softmax of tile X, key tile j: wait for S_X(j), load the whole row into
 // registers and release S at once, so the tensor core computes the other
-// tile's S while this softmax still works on j.  Row max (keys past the row's position
-// skipped on diagonal tiles); p = 2^(s*scale*log2e - m) (one FMA, one ex2)
+// tile's S while this softmax still works on j.  Row max: returned by the
+// loads themselves (tcgen05.ld.red) on tiles with no masked key, taken over
+// the unmasked keys on diagonal tiles; p = 2^(s*scale*log2e - m) (one FMA, one ex2)
 // packed to fp16 in registers with the row sum; then wait for P_X(j-1) V_{j-1}
 // (so O_X is stable and P_X free), rescale O_X only when the row max grew by
 // more than 2^8 (P then stays <= 256, exact in fp16 range), store P_X to
