@@ -5,6 +5,7 @@ CUDA kernels.  PyTorch supplies device memory and streams.  If the compiled
 library is missing the first call raises; there is no fallback.
 """
 import ctypes
+import functools
 import os
 
 import torch
@@ -166,6 +167,30 @@ def _io(t, dtype, name, ndim):
     return _ptr(t)
 
 
+def _one_device(fn):
+    """All CUDA tensors and streams of a call on one device, and the call made
+    with that device current: the library sets up and launches its kernels on
+    the current device."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        devs = set()
+        for a in list(args) + list(kwargs.values()):
+            if isinstance(a, torch.Tensor) and a.is_cuda:
+                devs.add(a.device)
+            elif isinstance(a, torch.cuda.Stream):
+                devs.add(a.device)
+        if len(devs) > 1:
+            raise ValueError(f"{fn.__name__}: CUDA tensors or streams on different devices: "
+                             + ", ".join(sorted(str(d) for d in devs)))
+        if devs:
+            dev = devs.pop()
+            if torch.cuda.current_device() != dev.index:
+                with torch.cuda.device(dev):
+                    return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return call
+
+
 def pa_decode_partition_tokens(B, H, block_size, max_context_len):
     return lib().pa_decode_partition_tokens(B, H, block_size, max_context_len)
 
@@ -175,6 +200,7 @@ def pa_decode_workspace_size(B, H, D, block_size, max_context_len, partition_tok
                                           partition_tokens)
 
 
+@_one_device
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
               out=None, partition_tokens=0, workspace=None, status=None, stream=None):
     """Paged decode attention.  q [B,H,D] fp16; caches [NB,bs,H,D] fp16;
@@ -211,6 +237,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_contex
     return out
 
 
+@_one_device
 def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
                      max_context_len, out=None, partition_tokens=0, workspace=None, status=None,
                      stream=None):
@@ -250,6 +277,7 @@ def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_le
     return out
 
 
+@_one_device
 def pa_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, seq_group,
                             group_offsets, group_seqs, group_prefix_len, scale, max_context_len,
                             max_group_size, max_prefix_len, out=None, partition_tokens=0,
@@ -313,6 +341,7 @@ def pa_shared_prefix_groups(block_tables, context_lens, block_size, min_shared_t
     return seq_group, offsets, seqs[:int(offsets[-1])].clone(), plen[:G].clone()
 
 
+@_one_device
 def pa_kv_cache_write_fp8(k, v, slot_mapping, k_cache8, v_cache8, k_scale, v_scale, status=None,
                           stream=None):
     """Quantize k/v [T,H,D] fp16 into e4m3 pools k_cache8/v_cache8
@@ -335,6 +364,7 @@ def pa_kv_cache_write_fp8(k, v, slot_mapping, k_cache8, v_cache8, k_scale, v_sca
     _check(rc, "pa_kv_cache_write_fp8")
 
 
+@_one_device
 def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_lens, scale,
                   max_context_len, out=None, partition_tokens=0, workspace=None, status=None,
                   stream=None):
@@ -372,6 +402,7 @@ def pa_prefill_workspace_size(B, H, Lq, D):
     return int(lib().pa_prefill_workspace_size(int(B), int(H), int(Lq), int(D)))
 
 
+@_one_device
 def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                      workspace=None, tail_split=True, status=None, stream=None, q_lens=None):
     """Chunked prefill attention.  q [B,H,Lq,D] fp16 are the last Lq positions
@@ -421,6 +452,7 @@ def pa_prefill_chunk(q, k_cache, v_cache, block_tables, context_lens, scale, out
     return out
 
 
+@_one_device
 def pa_prefill_chunk_varlen(q, k_cache, v_cache, block_tables, context_lens, q_lens, scale,
                             out=None, workspace=None, tail_split=True, status=None,
                             stream=None):
@@ -432,6 +464,7 @@ def pa_prefill_chunk_varlen(q, k_cache, v_cache, block_tables, context_lens, q_l
                             stream=stream, q_lens=q_lens)
 
 
+@_one_device
 def pa_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, status=None, stream=None):
     """Scatter k/v [T,H,D] fp16 into the caches at slot_mapping [T] int64."""
     _need(k, torch.float16, "k", 3)
@@ -451,6 +484,7 @@ def pa_kv_cache_write(k, v, slot_mapping, k_cache, v_cache, status=None, stream=
     _check(rc, "pa_kv_cache_write")
 
 
+@_one_device
 def pa_block_copy(k_cache, v_cache, pairs, status=None, stream=None):
     """Copy whole physical blocks: pairs [N,2] int64 (src, dst)."""
     _need(k_cache, torch.float16, "k_cache", 4)

@@ -124,9 +124,19 @@ class DecodeSession:
 
     def step_from_host(self, host, status=None, stream=None):
         """One decode step from the pinned host buffers of host_buffers(); the
-        output lands in host['out'] when the stream reaches the end."""
+        output lands in host['out'] when the stream reaches the end.  Runs
+        with the session's device current (the library launches there)."""
         if self._h_stage is None or host["q"].data_ptr() != self._h_stage.data_ptr():
             raise ValueError("step_from_host takes the buffers returned by host_buffers()")
+        dev = self.k_cache.device
+        if stream is not None and stream.device != dev:
+            raise ValueError(f"stream on {stream.device}, session on {dev}")
+        if torch.cuda.current_device() != dev.index:
+            with torch.cuda.device(dev):
+                return self._step(host, status, stream)
+        return self._step(host, status, stream)
+
+    def _step(self, host, status, stream):
         if stream is None:
             stream = torch.cuda.current_stream(self.k_cache.device)
         st = ctypes.c_void_p(None if status is None else status.data_ptr())
